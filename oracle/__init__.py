@@ -1,0 +1,183 @@
+"""fp64 CPU oracle for the fused DW/dense k x k -> 1x1 convolution module.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` are the only callers.  The product path (the CUDA library in
+``pointwise_conv_cnn_gb300``) never imports this package, and this package imports nothing
+from it.
+
+The arithmetic lives in ``fcm_oracle.c`` (plain loops, fp64).  This module only builds that
+file with gcc, loads it with ctypes and marshals numpy arrays.  Inputs of any float dtype are
+upcast to float64 exactly before the call; outputs are float64.
+
+Definitions followed (see the C file for the full list): "Fusing Depthwise and Pointwise
+Convolutions for Efficient Inference on GPUs", section II-B (DW and PW convolutions) and
+section III-A (conv -> norm -> activation, up to six fused layers); "Fusing two back-to-back
+convolutions" (CUTLASS discussion #208), the CONV1 3x3 -> CONV2 1x1 scale_bias_relu example.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fcm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACT = {"none": 0, "relu": 1, "relu6": 2}
+MID = {"exact": 0, "f32": 1, "f16": 2, "bf16": 3}
+
+
+def build(force: bool = False) -> str:
+    """Compile fcm_oracle.c into liboracle.so next to it (OpenMP when gcc supports it)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def bind(path: str):
+    """Load an oracle shared library from `path` and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    i = ctypes.c_int
+    lib.oracle_dw.argtypes = [i] * 7 + [dp] * 4 + [i, dp, i]
+    lib.oracle_pw.argtypes = [i] * 5 + [dp] * 4 + [i, dp, i]
+    lib.oracle_dense.argtypes = [i] * 8 + [dp] * 4 + [i, dp, i]
+    lib.oracle_fused.argtypes = [i] * 10 + [dp] * 4 + [i] + [dp] * 3 + [i, i, dp, i]
+    lib.oracle_round_format.argtypes = [ctypes.c_double, i, i, ctypes.c_double]
+    lib.oracle_round_format.restype = ctypes.c_double
+    lib.oracle_max_threads.argtypes = [i]
+    for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused,
+              lib.oracle_max_threads):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load(lib=None):
+    global _lib
+    if lib is not None:
+        return lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = bind(_LIB)
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def out_extent(n: int, k: int, s: int, p: int) -> int:
+    """Output extent floor((n + 2p - k)/s) + 1 (zero padding, cross-correlation)."""
+    return (n + 2 * p - k) // s + 1
+
+
+def max_threads(nthreads: int = 0, lib=None) -> int:
+    return int(_load(lib).oracle_max_threads(int(nthreads)))
+
+
+def dw(x, wd, s1, b1, act1="none", stride=1, pad=0, nthreads=0, lib=None) -> np.ndarray:
+    """Depthwise conv: x [N,H,W,C], wd [C,k,k] -> act1(s1*conv + b1) as [N,Ho,Wo,C]."""
+    x, wd, s1, b1 = map(_f64, (x, wd, s1, b1))
+    N, H, W, C = x.shape
+    k = wd.shape[1]
+    assert wd.shape == (C, k, k) and s1.shape == (C,) and b1.shape == (C,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    m = np.empty((N, Ho, Wo, C), np.float64)
+    rc = _load(lib).oracle_dw(N, H, W, C, k, stride, pad, _ptr(x), _ptr(wd), _ptr(s1), _ptr(b1),
+                           ACT[act1], _ptr(m), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_dw: invalid shape")
+    return m
+
+
+def pw(m, wp, s2, b2, act2="none", nthreads=0, lib=None) -> np.ndarray:
+    """Pointwise conv: m [N,Ho,Wo,Cm], wp [K,Cm] -> act2(s2*(m.wp^T) + b2) as [N,Ho,Wo,K]."""
+    m, wp, s2, b2 = map(_f64, (m, wp, s2, b2))
+    N, Ho, Wo, Cm = m.shape
+    K = wp.shape[0]
+    assert wp.shape == (K, Cm) and s2.shape == (K,) and b2.shape == (K,)
+    y = np.empty((N, Ho, Wo, K), np.float64)
+    rc = _load(lib).oracle_pw(N, Ho, Wo, Cm, K, _ptr(m), _ptr(wp), _ptr(s2), _ptr(b2), ACT[act2],
+                           _ptr(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pw: invalid shape")
+    return y
+
+
+def dense(x, w1, s1, b1, act1="none", stride=1, pad=0, nthreads=0, lib=None) -> np.ndarray:
+    """Dense conv: x [N,H,W,C], w1 [K1,k,k,C] -> act1(s1*conv + b1) as [N,Ho,Wo,K1]."""
+    x, w1, s1, b1 = map(_f64, (x, w1, s1, b1))
+    N, H, W, C = x.shape
+    K1, k = w1.shape[0], w1.shape[1]
+    assert w1.shape == (K1, k, k, C) and s1.shape == (K1,) and b1.shape == (K1,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    m = np.empty((N, Ho, Wo, K1), np.float64)
+    rc = _load(lib).oracle_dense(N, H, W, C, K1, k, stride, pad, _ptr(x), _ptr(w1), _ptr(s1),
+                              _ptr(b1), ACT[act1], _ptr(m), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_dense: invalid shape")
+    return m
+
+
+def fused(x, w1, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1, pad=0,
+          conv1="dw", mid="exact", nthreads=0, lib=None) -> np.ndarray:
+    """Fused module in one pass: conv1 (``"dw"`` with w1 [C,k,k] or ``"dense"`` with
+    w1 [K1,k,k,C]) + scale/bias/act1, then 1x1 conv wp [K,Cm] + scale/bias/act2."""
+    x, w1, s1, b1, wp, s2, b2 = map(_f64, (x, w1, s1, b1, wp, s2, b2))
+    N, H, W, C = x.shape
+    is_dense = conv1 == "dense"
+    if is_dense:
+        Cm, k = w1.shape[0], w1.shape[1]
+        assert w1.shape == (Cm, k, k, C)
+    else:
+        Cm, k = C, w1.shape[1]
+        assert w1.shape == (C, k, k)
+    K = wp.shape[0]
+    assert wp.shape == (K, Cm) and s1.shape == (Cm,) and b1.shape == (Cm,)
+    assert s2.shape == (K,) and b2.shape == (K,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    y = np.empty((N, Ho, Wo, K), np.float64)
+    rc = _load(lib).oracle_fused(int(is_dense), N, H, W, C, Cm, K, k, stride, pad, _ptr(x),
+                              _ptr(w1), _ptr(s1), _ptr(b1), ACT[act1], _ptr(wp), _ptr(s2),
+                              _ptr(b2), ACT[act2], MID[mid], _ptr(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_fused: invalid shape")
+    return y
+
+
+def round_format(v: float, prec: int, emin: int, maxf: float, lib=None) -> float:
+    """Round to nearest, ties to even, into a binary format (used by the mirror mode)."""
+    return float(_load(lib).oracle_round_format(float(v), prec, emin, float(maxf)))
+
+
+def build_variant(src_text: str, out_path: str) -> str:
+    """Compile C source text (e.g. a deliberately mutated copy of fcm_oracle.c, used by the
+    tests that show the pins catch planted mistakes) into `out_path`."""
+    c_path = out_path[:-3] + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", c_path, "-o", out_path, "-lm"],
+                   check=True, capture_output=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()

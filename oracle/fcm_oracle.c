@@ -1,0 +1,248 @@
+/*
+ * fcm_oracle.c -- plain, slow, fp64 CPU oracle for the fused depthwise/dense k x k -> 1x1
+ * pointwise convolution module.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and its Python
+ * binding) links, loads or calls this file.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or helper with
+ * the CUDA kernels.
+ *
+ * What it computes, and where the pages define it:
+ *  - Depthwise (DW) convolution: one k x k filter per channel, applied over height and
+ *    width ("Fusing Depthwise and Pointwise Convolutions for Efficient Inference on GPUs",
+ *    section II-B, Figure 2).
+ *  - Pointwise (PW) convolution: 1x1 filters spanning all channels (same section).
+ *  - A depthwise separable convolution is a DW layer followed by a PW layer (same section).
+ *  - Each convolution is followed by its normalization and activation layers; an FCM fuses
+ *    up to six layers: two convolutions, each with its norm and activation (section III-A).
+ *    With inference-time batch norm folded, norm is a per-channel scale and bias.
+ *  - Back-to-back case: a dense 3x3 convolution followed by a 1x1 convolution, each with a
+ *    per-channel scale_bias_relu epilogue, NHWC activations ("Fusing two back-to-back
+ *    convolutions", CUTLASS discussion #208, the CONV1/CONV2 example).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - zero padding; output size Ho = floor((H + 2p - k) / s) + 1, likewise Wo;
+ *  - cross-correlation (no filter flip), output (ho, wo) reads input rows ho*s-p .. ho*s-p+k-1;
+ *  - norm+act form is act(scale[c] * acc + bias[c]);
+ *  - ReLU = max(v, 0), ReLU6 = min(max(v, 0), 6), none = v;
+ *  - the intermediate is kept in fp64 unless a "mirror" rounding of it to the GPU storage
+ *    format is requested (used only for diagnosis, never for the parity bar).
+ *
+ * Layouts (all row-major, innermost last):
+ *   x  [N][H][W][C]           input feature maps (NHWC)
+ *   wd [C][k][k]              depthwise filters
+ *   w1 [K1][k][k][C]          dense conv1 filters (K, R, S, C)
+ *   wp [K][Cm]                pointwise filters (Cm = C for DW, K1 for dense)
+ *   m  [N][Ho][Wo][Cm]        intermediate feature maps
+ *   y  [N][Ho][Wo][K]         output feature maps
+ *
+ * Every function returns 0 on success and -1 on an invalid shape.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_RELU6 = 2 };
+enum { ORACLE_MID_EXACT = 0, ORACLE_MID_F32 = 1, ORACLE_MID_F16 = 2, ORACLE_MID_BF16 = 3 };
+
+/* Activation after the folded norm (section III-A: conv -> norm -> activation). */
+static double act_apply(double v, int act) {
+    if (act == ORACLE_ACT_RELU) return v > 0.0 ? v : 0.0;
+    if (act == ORACLE_ACT_RELU6) {
+        if (v < 0.0) return 0.0;
+        if (v > 6.0) return 6.0;
+        return v;
+    }
+    return v;
+}
+
+/*
+ * Round v to the nearest value of a binary floating-point format with `prec` significand
+ * bits (implicit bit included), minimum normal exponent `emin` and largest finite value
+ * `maxf`, ties to even (IEEE 754 roundTiesToEven).  Values past the largest finite one
+ * round to infinity.  f16: prec 11, emin -14.  bf16: prec 8, emin -126.
+ */
+double oracle_round_format(double v, int prec, int emin, double maxf) {
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    (void)frexp(v, &e);          /* v = f * 2^e with 0.5 <= |f| < 1: leading bit is 2^(e-1) */
+    int lead = e - 1;
+    if (lead < emin) lead = emin; /* subnormal range: fixed quantum 2^(emin - prec + 1) */
+    double quantum = ldexp(1.0, lead - (prec - 1));
+    double r = nearbyint(v / quantum) * quantum; /* exact scaling; nearbyint ties to even */
+    if (fabs(r) > maxf) r = copysign(INFINITY, v);
+    return r;
+}
+
+static double mid_round(double v, int mid_mode) {
+    switch (mid_mode) {
+    case ORACLE_MID_F32: return (double)(float)v;
+    case ORACLE_MID_F16: return oracle_round_format(v, 11, -14, 65504.0);
+    case ORACLE_MID_BF16: return oracle_round_format(v, 8, -126, ldexp(255.0, 120));
+    default: return v;
+    }
+}
+
+static int out_extent(int in, int k, int s, int p) {
+    if (k < 1 || s < 1 || p < 0 || in + 2 * p < k) return -1;
+    return (in + 2 * p - k) / s + 1;
+}
+
+#define IDX4(a, b, c, d, B, C, D) ((((size_t)(a) * (B) + (b)) * (C) + (c)) * (D) + (d))
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* Threads the OpenMP runtime will use for the next parallel region (1 without OpenMP). */
+int oracle_max_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) return nthreads;
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* Depthwise k x k convolution + per-channel scale/bias + activation (section II-B). */
+int oracle_dw(int N, int H, int W, int C, int k, int s, int p,
+              const double *x, const double *wd, const double *s1, const double *b1, int act1,
+              double *m, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int c = 0; c < C; c++) {
+                    double t = 0.0;
+                    for (int i = 0; i < k; i++) {
+                        int hi = ho * s - p + i;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int j = 0; j < k; j++) {
+                            int wi = wo * s - p + j;
+                            if (wi < 0 || wi >= W) continue;
+                            t += x[IDX4(n, hi, wi, c, H, W, C)] * wd[((size_t)c * k + i) * k + j];
+                        }
+                    }
+                    m[IDX4(n, ho, wo, c, Ho, Wo, C)] = act_apply(s1[c] * t + b1[c], act1);
+                }
+    return 0;
+}
+
+/* Pointwise 1x1 convolution + per-channel scale/bias + activation (section II-B). */
+int oracle_pw(int N, int Ho, int Wo, int Cm, int K,
+              const double *m, const double *wp, const double *s2, const double *b2, int act2,
+              double *y, int nthreads) {
+    if (N < 0 || Ho < 1 || Wo < 1 || Cm < 1 || K < 1) return -1;
+    set_threads(nthreads);
+    long long P = (long long)N * Ho * Wo;
+#pragma omp parallel for schedule(static)
+    for (long long q = 0; q < P; q++)
+        for (int kk = 0; kk < K; kk++) {
+            double t = 0.0;
+            for (int c = 0; c < Cm; c++) t += m[(size_t)q * Cm + c] * wp[(size_t)kk * Cm + c];
+            y[(size_t)q * K + kk] = act_apply(s2[kk] * t + b2[kk], act2);
+        }
+    return 0;
+}
+
+/* Dense k x k convolution C -> K1 + per-channel scale/bias + activation (CONV1 of the
+ * back-to-back example). */
+int oracle_dense(int N, int H, int W, int C, int K1, int k, int s, int p,
+                 const double *x, const double *w1, const double *s1, const double *b1, int act1,
+                 double *m, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || K1 < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int j = 0; j < K1; j++) {
+                    double t = 0.0;
+                    for (int r = 0; r < k; r++) {
+                        int hi = ho * s - p + r;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int u = 0; u < k; u++) {
+                            int wi = wo * s - p + u;
+                            if (wi < 0 || wi >= W) continue;
+                            for (int c = 0; c < C; c++)
+                                t += x[IDX4(n, hi, wi, c, H, W, C)] *
+                                     w1[IDX4(j, r, u, c, k, k, C)];
+                        }
+                    }
+                    m[IDX4(n, ho, wo, j, Ho, Wo, K1)] = act_apply(s1[j] * t + b1[j], act1);
+                }
+    return 0;
+}
+
+/*
+ * The fused module, written as its own single pass: for every output pixel, the first
+ * convolution (DW, or dense when `dense` is non-zero) produces that pixel's intermediate
+ * vector over all channels, which is then consumed at once by the 1x1 convolution -- the
+ * "all channels of the intermediate" requirement of the DWPW case (section II-D).  It does
+ * not call oracle_dw/oracle_pw, so comparing the two is a real check.
+ * mid_mode: 0 keep the intermediate exact (fp64); 1/2/3 round it to f32/f16/bf16 first.
+ */
+int oracle_fused(int dense, int N, int H, int W, int C, int Cm, int K, int k, int s, int p,
+                 const double *x, const double *w1, const double *s1, const double *b1, int act1,
+                 const double *wp, const double *s2, const double *b2, int act2,
+                 int mid_mode, double *y, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Cm < 1 || K < 1 || Ho < 1 || Wo < 1) return -1;
+    if (!dense && Cm != C) return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *mid = (double *)malloc(sizeof(double) * (size_t)Cm);
+        if (!mid) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for collapse(2) schedule(static)
+        for (int n = 0; n < N; n++)
+            for (int ho = 0; ho < Ho; ho++) {
+                if (!mid) continue;
+                for (int wo = 0; wo < Wo; wo++) {
+                    for (int j = 0; j < Cm; j++) {
+                        double t = 0.0;
+                        for (int r = 0; r < k; r++) {
+                            int hi = ho * s - p + r;
+                            if (hi < 0 || hi >= H) continue;
+                            for (int u = 0; u < k; u++) {
+                                int wi = wo * s - p + u;
+                                if (wi < 0 || wi >= W) continue;
+                                if (dense) {
+                                    for (int c = 0; c < C; c++)
+                                        t += x[IDX4(n, hi, wi, c, H, W, C)] *
+                                             w1[IDX4(j, r, u, c, k, k, C)];
+                                } else {
+                                    t += x[IDX4(n, hi, wi, j, H, W, C)] *
+                                         w1[((size_t)j * k + r) * k + u];
+                                }
+                            }
+                        }
+                        mid[j] = mid_round(act_apply(s1[j] * t + b1[j], act1), mid_mode);
+                    }
+                    for (int kk = 0; kk < K; kk++) {
+                        double t = 0.0;
+                        for (int j = 0; j < Cm; j++) t += mid[j] * wp[(size_t)kk * Cm + j];
+                        y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = act_apply(s2[kk] * t + b2[kk], act2);
+                    }
+                }
+            }
+        free(mid);
+    }
+    return failed ? -1 : 0;
+}
