@@ -1,0 +1,177 @@
+/*
+ * fcm.h -- C ABI of the fused convolutional module (FCM) library for GB300 (sm_103a).
+ *
+ * One call runs a block-resident fused pair of convolutions on NHWC activations:
+ *
+ *     m = act1(s1 * conv1(x) + b1)          conv1: depthwise k x k, or dense k x k
+ *     y = act2(s2 * (m . wp^T) + b2)        1x1 pointwise convolution
+ *
+ * where the intermediate m never leaves the thread block (shared memory / tensor memory).
+ * Definitions: "Fusing Depthwise and Pointwise Convolutions for Efficient Inference on GPUs",
+ * section II-B (DW and PW convolutions), section II-D (the DWPW tile must hold all channels),
+ * section III (FCMs: up to six fused layers -- two convolutions, each followed by its
+ * normalization and activation -- with the intermediate kept in a shared "commBuffer"), and
+ * section IV (FusePlanner cost models, Equations 1-4).  The dense case follows "Fusing two
+ * back-to-back convolutions" (CUTLASS discussion #208): the second convolution must be 1x1 so
+ * that a block never needs another block's intermediate.
+ *
+ * Conventions for every entry point:
+ *  - Status codes only: no exception, abort or exit crosses the ABI.  A human-readable
+ *    message for the last failure on the calling thread is returned by fcm_last_error().
+ *  - Activations are NHWC, contiguous, of the handle's dtype, 16-byte aligned, in device
+ *    memory owned by the caller (except fcm_run_host, which takes host memory).
+ *  - Scales and biases are float32.  Weights are of the handle's dtype.
+ *  - Arithmetic: products and sums in fp32 (fp16/bf16 storage widened exactly); the
+ *    intermediate is rounded to the storage dtype (round to nearest even) before the 1x1
+ *    convolution consumes it; the output is rounded to the storage dtype.
+ *  - Zero padding, cross-correlation (no filter flip):
+ *    Ho = (H + 2*pad - ksize) / stride + 1, likewise Wo.
+ */
+#ifndef FCM_H
+#define FCM_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FCM_API __attribute__((visibility("default")))
+#else
+#define FCM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fcm_status {
+    FCM_OK = 0,
+    FCM_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, bad enum value */
+    FCM_ERR_UNSUPPORTED = 2,   /* valid request this library does not implement */
+    FCM_ERR_ALIGNMENT = 3,     /* activation pointer not 16-byte aligned */
+    FCM_ERR_SMEM_BUDGET = 4,   /* no tile fits in shared memory */
+    FCM_ERR_CUDA = 5,          /* a CUDA runtime call failed (message has the CUDA error) */
+    FCM_ERR_TIMEOUT = 6,       /* a kernel's bounded wait ran out (reported by fcm_check) */
+    FCM_ERR_DEVICE_FAULT = 7,  /* a kernel's own consistency check failed (fcm_check) */
+    FCM_ERR_NO_DEVICE = 8      /* no CUDA device, or not a compute capability 10.3 device */
+} fcm_status;
+
+typedef enum fcm_dtype { FCM_F32 = 0, FCM_F16 = 1, FCM_BF16 = 2 } fcm_dtype;
+typedef enum fcm_act { FCM_ACT_NONE = 0, FCM_ACT_RELU = 1, FCM_ACT_RELU6 = 2 } fcm_act;
+typedef enum fcm_conv1_kind { FCM_CONV1_DEPTHWISE = 0, FCM_CONV1_DENSE = 1 } fcm_conv1_kind;
+
+/* What fcm_run computes.  The three non-fused modes are the layer-by-layer (LBL) baselines of
+ * the paper's section V-C, built from the same building blocks as the fused kernels. */
+typedef enum fcm_mode {
+    FCM_MODE_FUSED = 0,       /* in = x [N,H,W,C]    -> out = y [N,Ho,Wo,K]                 */
+    FCM_MODE_CONV1_ONLY = 1,  /* in = x [N,H,W,C]    -> out = m [N,Ho,Wo,Cm] (storage dtype) */
+    FCM_MODE_PW_ONLY = 2,     /* in = m [N,Ho,Wo,Cm] -> out = y [N,Ho,Wo,K]                 */
+    FCM_MODE_UNFUSED = 3      /* CONV1_ONLY then PW_ONLY through an intermediate buffer the
+                                 handle allocates on first use and owns                     */
+} fcm_mode;
+
+/* Kernel family request.  AUTO picks the tensor-core (tcgen05) kernels whenever the shape
+ * is supported by them, else the CUDA-core (SIMT) kernels.  fp32 always runs SIMT. */
+typedef enum fcm_kernel_pref { FCM_KERNEL_AUTO = 0, FCM_KERNEL_SIMT = 1, FCM_KERNEL_TC = 2 } fcm_kernel_pref;
+
+typedef struct fcm_desc {
+    int n, h, w, c;        /* input feature maps, NHWC                                     */
+    int k_out;             /* 1x1 convolution output channels K                             */
+    int mid;               /* dense conv1 output channels Cm (0 = C); must be 0 or C for DW */
+    int ksize, stride, pad;/* conv1 filter size, stride, zero padding (square)              */
+    int conv1;             /* fcm_conv1_kind                                                */
+    int dtype;             /* fcm_dtype of activations and weights                          */
+    int act1, act2;        /* fcm_act after conv1 and after the 1x1 convolution             */
+    int tile_h, tile_w;    /* output tile override (0 = the planner chooses)                */
+    int kernel;            /* fcm_kernel_pref                                               */
+} fcm_desc;
+
+/* What the tile planner chose, and the byte counts it compared (section IV). */
+typedef struct fcm_plan_info {
+    int ho, wo, cm;
+    int kernel;                  /* 1 = SIMT kernels, 2 = tcgen05 kernels                     */
+    int tile_h, tile_w;          /* output tile (pixels), all channels (section II-D rule)    */
+    int chunk_c;                 /* conv1 channels per pipeline stage                         */
+    int stages;                  /* input pipeline depth                                      */
+    int ctas;                    /* persistent grid size                                      */
+    int threads;                 /* threads per CTA                                           */
+    int smem_bytes;              /* dynamic shared memory per CTA                             */
+    long long num_tiles;         /* output tiles over the whole batch                         */
+    long long bytes_fused_min;   /* input + weights + scale/bias + output, each once          */
+    long long bytes_unfused_min; /* the above + one write and one read of the intermediate    */
+    long long gma_fused_model;   /* DWPW estimator built from Eq. 1-3, bytes, whole batch     */
+    long long gma_lbl_model;     /* Eq. 3 (DW) + Eq. 2 (PW), bytes, whole batch               */
+    long long overlap_elems;     /* Eq. 1 for the chosen tile, elements per channel per image */
+} fcm_plan_info;
+
+typedef struct fcm_handle fcm_handle;
+
+/* Create a module.  w1: DW filters [C][k][k] or dense filters [Cm][k][k][C]; wp: 1x1 filters
+ * [K][Cm]; s1,b1: [Cm]; s2,b2: [K].  Each pointer may be host or device memory (unified
+ * addressing decides); the handle copies and repacks everything into device memory it owns,
+ * so the caller may free its copies on return.  Rejects (FCM_ERR_UNSUPPORTED) a second
+ * convolution that is not 1x1 by construction: there is no parameter for it.  Uses the
+ * current CUDA device; every later call on the handle must run with that device current.
+ * On failure *out is set to NULL. */
+FCM_API fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp,
+                      const float *s1, const float *b1, const float *s2, const float *b2,
+                      fcm_handle **out);
+
+/* Enqueue one evaluation on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * `in`/`out` are caller-owned device pointers as described by fcm_mode; they must not
+ * overlap.  Asynchronous: returns after the launch; launch errors are reported here, errors
+ * found by the kernel itself are reported by fcm_check. */
+FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, void *stream);
+
+/* End-to-end variant of fcm_run on HOST buffers: copies `host_in` to a device staging buffer
+ * owned by the handle (allocated on first use), runs `mode`, copies the result to `host_out`
+ * and synchronizes `stream` before returning.  Pinned host memory makes the copies faster;
+ * pageable memory also works. */
+FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
+                        void *stream);
+
+/* Synchronize `stream`, then read and clear the handle's device error word.  Returns
+ * FCM_ERR_TIMEOUT if a bounded wait in a kernel ran out, FCM_ERR_DEVICE_FAULT if a kernel's
+ * own check failed, FCM_OK otherwise. */
+FCM_API fcm_status fcm_check(fcm_handle *h, void *stream);
+
+/* The plan of an existing handle. */
+FCM_API fcm_status fcm_plan(const fcm_handle *h, fcm_plan_info *info);
+
+/* Run the tile planner for a descriptor without a GPU: `num_sms` and `smem_per_block` (bytes
+ * of opt-in dynamic shared memory per CTA) describe the target (152 and 232448 on GB300). */
+FCM_API fcm_status fcm_plan_desc(const fcm_desc *desc, int num_sms, int smem_per_block,
+                         fcm_plan_info *info);
+
+/* Size in bytes of each tensor of a descriptor: x, m (intermediate), y. */
+FCM_API fcm_status fcm_tensor_bytes(const fcm_desc *desc, size_t *x_bytes, size_t *m_bytes,
+                            size_t *y_bytes);
+
+/* Free the handle and everything it owns (waits for the device).  NULL is ignored. */
+FCM_API void fcm_destroy(fcm_handle *h);
+
+/* Message of the last failing call on this thread ("" if none).  Valid until the next call. */
+FCM_API const char *fcm_last_error(void);
+
+/* ---- FusePlanner cost models, section IV (element counts per image; exported for tests). */
+/* Eq. 1: halo elements per channel re-read across tiles. */
+FCM_API long long fcm_model_overlap(long long channel_w, long long channel_h, long long tile_w,
+                            long long tile_h, long long filter_w, long long filter_h,
+                            long long strides);
+/* Eq. 2: PW layer-by-layer global memory accesses. */
+FCM_API long long fcm_model_pw_gma(long long weights_sz, long long weights_tile_sz, long long ifms_sz,
+                           long long ofms_sz, long long ofms_tile_sz);
+/* Eq. 3: DW layer-by-layer global memory accesses. */
+FCM_API long long fcm_model_dw_gma(long long ifms_d, long long overlap, long long ifms_sz,
+                           long long ofms_sz, long long ofms_hw, long long ofms_tile_hw,
+                           long long weights_sz);
+/* DWPW FCM estimator, built from Eq. 2 and 3 the way section IV-B builds Eq. 4:
+ * (2*C*Overlap + DwIFMsSz) * ceil(PwWeightsSz/PwWeightsTileSz) + PwOFMsSz
+ *   + ceil(OFMsHW/OFMsTileHW) * (DwWeightsSz + PwWeightsSz). */
+FCM_API long long fcm_model_dwpw_gma(long long c, long long overlap, long long dw_ifms_sz,
+                             long long pw_weights_sz, long long pw_weights_tile_sz,
+                             long long pw_ofms_sz, long long ofms_hw, long long ofms_tile_hw,
+                             long long dw_weights_sz);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FCM_H */

@@ -1,0 +1,253 @@
+"""Thin Python binding of the FCM C ABI (``include/fcm.h``) for GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels of
+``libfcm.so``.  PyTorch provides device memory and streams (``tensor.data_ptr()``,
+``torch.cuda.current_stream().cuda_stream``); nothing here computes on the CPU, and a missing
+library raises instead of falling back.
+
+The functions keep the C names (``fcm_create``, ``fcm_run``, ...).  ``FusedConvModule`` wraps
+a handle for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "FCM_OK", "FcmError", "FcmDesc", "FcmPlanInfo", "FusedConvModule", "load_library",
+    "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
+    "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
+    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "EXPORTED_SYMBOLS",
+    "DTYPES", "ACTS", "MODES",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfcm.so")
+
+FCM_OK = 0
+STATUS_NAMES = {0: "FCM_OK", 1: "FCM_ERR_INVALID_ARG", 2: "FCM_ERR_UNSUPPORTED",
+                3: "FCM_ERR_ALIGNMENT", 4: "FCM_ERR_SMEM_BUDGET", 5: "FCM_ERR_CUDA",
+                6: "FCM_ERR_TIMEOUT", 7: "FCM_ERR_DEVICE_FAULT", 8: "FCM_ERR_NO_DEVICE"}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+ACTS = {"none": 0, "relu": 1, "relu6": 2}
+CONV1 = {"dw": 0, "dense": 1}
+MODES = {"fused": 0, "conv1": 1, "pw": 2, "unfused": 3}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+
+EXPORTED_SYMBOLS = (
+    "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
+    "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
+    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma",
+)
+
+
+class FcmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+class FcmDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "n", "h", "w", "c", "k_out", "mid", "ksize", "stride", "pad", "conv1", "dtype", "act1",
+        "act2", "tile_h", "tile_w", "kernel")]
+
+
+class FcmPlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "ho", "wo", "cm", "kernel", "tile_h", "tile_w", "chunk_c", "stages", "ctas", "threads",
+        "smem_bytes")] + [(n, ctypes.c_longlong) for n in (
+            "num_tiles", "bytes_fused_min", "bytes_unfused_min", "gma_fused_model",
+            "gma_lbl_model", "overlap_elems")]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libfcm.so (built in-tree by ``pointwise_conv_cnn_gb300.build``).  Raises if the
+    library is missing: there is no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FileNotFoundError(
+                f"{p} is missing: build it with `python -m pointwise_conv_cnn_gb300.build`")
+        lib = ctypes.CDLL(p)
+        vp, i, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.fcm_create.argtypes = [ctypes.POINTER(FcmDesc), vp, vp, vp, vp, vp, vp,
+                                   ctypes.POINTER(vp)]
+        lib.fcm_run.argtypes = [vp, i, vp, vp, vp]
+        lib.fcm_run_host.argtypes = [vp, i, vp, vp, vp]
+        lib.fcm_check.argtypes = [vp, vp]
+        lib.fcm_plan.argtypes = [vp, ctypes.POINTER(FcmPlanInfo)]
+        lib.fcm_plan_desc.argtypes = [ctypes.POINTER(FcmDesc), i, i, ctypes.POINTER(FcmPlanInfo)]
+        lib.fcm_tensor_bytes.argtypes = [ctypes.POINTER(FcmDesc)] + [ctypes.POINTER(ctypes.c_size_t)] * 3
+        for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan",
+                  "fcm_plan_desc", "fcm_tensor_bytes"):
+            getattr(lib, f).restype = i
+        lib.fcm_destroy.argtypes = [vp]
+        lib.fcm_destroy.restype = None
+        lib.fcm_last_error.argtypes = []
+        lib.fcm_last_error.restype = ctypes.c_char_p
+        lib.fcm_model_overlap.argtypes = [ll] * 7
+        lib.fcm_model_pw_gma.argtypes = [ll] * 5
+        lib.fcm_model_dw_gma.argtypes = [ll] * 7
+        lib.fcm_model_dwpw_gma.argtypes = [ll] * 9
+        for f in ("fcm_model_overlap", "fcm_model_pw_gma", "fcm_model_dw_gma",
+                  "fcm_model_dwpw_gma"):
+            getattr(lib, f).restype = ll
+        del fp
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != FCM_OK:
+        raise FcmError(status, fcm_last_error())
+
+
+def fcm_last_error() -> str:
+    return load_library().fcm_last_error().decode(errors="replace")
+
+
+def make_desc(n, h, w, c, k_out, ksize, stride, pad, conv1="dw", dtype="f16", act1="relu",
+              act2="relu", mid=0, tile_h=0, tile_w=0, kernel="auto") -> FcmDesc:
+    return FcmDesc(n, h, w, c, k_out, mid, ksize, stride, pad, CONV1[conv1], DTYPES[dtype],
+                   ACTS[act1], ACTS[act2], tile_h, tile_w, KERNELS[kernel])
+
+
+def desc_from_workload(wl, **over) -> FcmDesc:
+    kw = dict(n=wl.n, h=wl.h, w=wl.w, c=wl.c, k_out=wl.k_out, ksize=wl.ksize, stride=wl.stride,
+              pad=wl.pad, conv1=wl.conv1, dtype=wl.dtype, act1=wl.act1, act2=wl.act2,
+              mid=wl.mid if wl.conv1 == "dense" else 0)
+    kw.update(over)
+    return make_desc(**kw)
+
+
+def fcm_create(desc: FcmDesc, w1: int, wp: int, s1: int, b1: int, s2: int, b2: int) -> int:
+    """Raw C call; pointers are integers (host or device addresses).  Returns the handle."""
+    out = ctypes.c_void_p()
+    _check(load_library().fcm_create(ctypes.byref(desc), w1, wp, s1, b1, s2, b2,
+                                     ctypes.byref(out)))
+    return out.value
+
+
+def fcm_run(handle: int, mode: int, inp: int, out: int, stream: int = 0) -> None:
+    _check(load_library().fcm_run(handle, mode, inp, out, stream))
+
+
+def fcm_run_host(handle: int, mode: int, host_in: int, host_out: int, stream: int = 0) -> None:
+    _check(load_library().fcm_run_host(handle, mode, host_in, host_out, stream))
+
+
+def fcm_check(handle: int, stream: int = 0) -> None:
+    _check(load_library().fcm_check(handle, stream))
+
+
+def fcm_plan(handle: int) -> dict:
+    info = FcmPlanInfo()
+    _check(load_library().fcm_plan(handle, ctypes.byref(info)))
+    return info.as_dict()
+
+
+def fcm_plan_desc(desc: FcmDesc, num_sms: int = 152, smem_per_block: int = 232448) -> dict:
+    info = FcmPlanInfo()
+    _check(load_library().fcm_plan_desc(ctypes.byref(desc), num_sms, smem_per_block,
+                                        ctypes.byref(info)))
+    return info.as_dict()
+
+
+def fcm_tensor_bytes(desc: FcmDesc) -> tuple[int, int, int]:
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load_library().fcm_tensor_bytes(ctypes.byref(desc), ctypes.byref(a),
+                                           ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def fcm_destroy(handle: int) -> None:
+    if handle:
+        load_library().fcm_destroy(handle)
+
+
+def fcm_model_overlap(*a) -> int:
+    return load_library().fcm_model_overlap(*a)
+
+
+def fcm_model_pw_gma(*a) -> int:
+    return load_library().fcm_model_pw_gma(*a)
+
+
+def fcm_model_dw_gma(*a) -> int:
+    return load_library().fcm_model_dw_gma(*a)
+
+
+def fcm_model_dwpw_gma(*a) -> int:
+    return load_library().fcm_model_dwpw_gma(*a)
+
+
+class FusedConvModule:
+    """Owns one FCM handle.  Weights are torch tensors or numpy arrays in the storage dtype
+    (bf16 may be given as uint16 bit patterns); scales/biases float32."""
+
+    def __init__(self, desc: FcmDesc, w1, wp, s1, b1, s2, b2):
+        import numpy as np
+        self.desc = desc
+        keep = []
+
+        def addr(a):
+            if hasattr(a, "data_ptr"):
+                t = a.contiguous()
+                keep.append(t)
+                return t.data_ptr()
+            arr = np.ascontiguousarray(a)
+            keep.append(arr)
+            return arr.ctypes.data
+
+        self.handle = fcm_create(desc, addr(w1), addr(wp), addr(s1), addr(b1), addr(s2),
+                                 addr(b2))
+        self.plan = fcm_plan(self.handle)
+
+    def run(self, inp, out, mode: str | int = "fused", stream=None) -> None:
+        """Enqueue on `stream` (torch.cuda.Stream, raw handle int, or None = current stream)."""
+        import torch
+        m = MODES[mode] if isinstance(mode, str) else mode
+        if stream is None:
+            s = torch.cuda.current_stream().cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            s = stream.cuda_stream
+        else:
+            s = int(stream)
+        fcm_run(self.handle, m, inp.data_ptr(), out.data_ptr(), s)
+
+    def run_host(self, host_in, host_out, mode: str | int = "fused", stream=None) -> None:
+        import torch
+        m = MODES[mode] if isinstance(mode, str) else mode
+        s = (torch.cuda.current_stream().cuda_stream if stream is None
+             else getattr(stream, "cuda_stream", stream))
+        fcm_run_host(self.handle, m, host_in.data_ptr(), host_out.data_ptr(), s)
+
+    def check(self, stream=None) -> None:
+        import torch
+        s = (torch.cuda.current_stream().cuda_stream if stream is None
+             else getattr(stream, "cuda_stream", stream))
+        fcm_check(self.handle, s)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            fcm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

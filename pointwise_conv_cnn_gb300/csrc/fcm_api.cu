@@ -1,0 +1,305 @@
+// fcm_api.cu -- the C ABI: argument checks, handle lifetime, weight repacking, dispatch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "fcm_internal.h"
+
+static thread_local char g_last_error[512] = "";
+
+fcm_status fcm_fail(fcm_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static fcm_status cuda_fail(cudaError_t e, const char *what) {
+    return fcm_fail(FCM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define FCM_CUDA(call)                                              \
+    do {                                                            \
+        cudaError_t e__ = (call);                                   \
+        if (e__ != cudaSuccess) return cuda_fail(e__, #call);       \
+    } while (0)
+
+// storage -> float on the host (CUDA's own host-side conversions)
+static float host_to_f(const void *base, size_t i, int dtype) {
+    switch (dtype) {
+    case FCM_F32: return static_cast<const float *>(base)[i];
+    case FCM_F16: return __half2float(static_cast<const __half *>(base)[i]);
+    default: return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[i]);
+    }
+}
+
+template <typename T>
+static fcm_status upload(T **dst, const T *src, size_t count) {
+    FCM_CUDA(cudaMalloc(reinterpret_cast<void **>(dst), count * sizeof(T)));
+    FCM_CUDA(cudaMemcpy(*dst, src, count * sizeof(T), cudaMemcpyHostToDevice));
+    return FCM_OK;
+}
+
+static fcm_status fetch(std::vector<unsigned char> &dst, const void *src, size_t bytes,
+                        const char *name) {
+    if (!src) return fcm_fail(FCM_ERR_INVALID_ARG, "%s is NULL", name);
+    dst.resize(bytes);
+    cudaError_t e = cudaMemcpy(dst.data(), src, bytes, cudaMemcpyDefault);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return FCM_OK;
+}
+
+static void free_handle(fcm_handle *h) {
+    if (!h) return;
+    void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->s1, h->b1,
+                    h->s2, h->b2, h->d_err, h->mid_buf, h->stage_in, h->stage_out};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+    delete h;
+}
+
+extern "C" {
+
+const char *fcm_last_error(void) { return g_last_error; }
+
+fcm_status fcm_tensor_bytes(const fcm_desc *desc, size_t *x_bytes, size_t *m_bytes,
+                            size_t *y_bytes) {
+    int ho, wo, cm;
+    fcm_status st = fcm_validate_desc(desc, &ho, &wo, &cm);
+    if (st != FCM_OK) return st;
+    size_t e = desc->dtype == FCM_F32 ? 4 : 2;
+    if (x_bytes) *x_bytes = (size_t)desc->n * desc->h * desc->w * desc->c * e;
+    if (m_bytes) *m_bytes = (size_t)desc->n * ho * wo * cm * e;
+    if (y_bytes) *y_bytes = (size_t)desc->n * ho * wo * desc->k_out * e;
+    return FCM_OK;
+}
+
+fcm_status fcm_plan_desc(const fcm_desc *desc, int num_sms, int smem_per_block,
+                         fcm_plan_info *info) {
+    return fcm_make_plan(desc, num_sms, smem_per_block, info, nullptr);
+}
+
+fcm_status fcm_plan(const fcm_handle *h, fcm_plan_info *info) {
+    if (!h || !info) return fcm_fail(FCM_ERR_INVALID_ARG, "handle or info is NULL");
+    *info = h->plan;
+    return FCM_OK;
+}
+
+fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, const float *s1,
+                      const float *b1, const float *s2, const float *b2, fcm_handle **out) {
+    if (!out) return fcm_fail(FCM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int ho, wo, cm;
+    fcm_status st = fcm_validate_desc(desc, &ho, &wo, &cm);
+    if (st != FCM_OK) return st;
+
+    int dev = 0, ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+        cudaGetLastError();
+        return fcm_fail(FCM_ERR_NO_DEVICE, "no CUDA device");
+    }
+    FCM_CUDA(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    FCM_CUDA(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3)
+        return fcm_fail(FCM_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a",
+                        dev, prop.major, prop.minor);
+
+    fcm_handle *h = new fcm_handle();
+    h->d = *desc;
+    h->device = dev;
+    h->ho = ho;
+    h->wo = wo;
+    h->cm = cm;
+    h->esize = desc->dtype == FCM_F32 ? 4 : 2;
+    h->num_sms = prop.multiProcessorCount;
+    h->smem_optin = (int)prop.sharedMemPerBlockOptin;
+    h->x_elems = (size_t)desc->n * desc->h * desc->w * desc->c;
+    h->m_elems = (size_t)desc->n * ho * wo * cm;
+    h->y_elems = (size_t)desc->n * ho * wo * desc->k_out;
+
+    st = fcm_make_plan(desc, h->num_sms, h->smem_optin, &h->plan, &h->tc);
+    if (st != FCM_OK) {
+        free_handle(h);
+        return st;
+    }
+
+    const int C = desc->c, K = desc->k_out, k = desc->ksize, dt = desc->dtype;
+    const bool dense = desc->conv1 == FCM_CONV1_DENSE;
+    const size_t n_w1 = dense ? (size_t)cm * k * k * C : (size_t)C * k * k;
+    const size_t n_wp = (size_t)K * cm;
+    std::vector<unsigned char> hw1, hwp, hs1, hb1, hs2, hb2;
+    if ((st = fetch(hw1, w1, n_w1 * h->esize, "w1")) != FCM_OK ||
+        (st = fetch(hwp, wp, n_wp * h->esize, "wp")) != FCM_OK ||
+        (st = fetch(hs1, s1, cm * 4, "s1")) != FCM_OK ||
+        (st = fetch(hb1, b1, cm * 4, "b1")) != FCM_OK ||
+        (st = fetch(hs2, s2, K * 4, "s2")) != FCM_OK ||
+        (st = fetch(hb2, b2, K * 4, "b2")) != FCM_OK) {
+        free_handle(h);
+        return st;
+    }
+
+    // SIMT layouts: conv1 taps major ([k*k][C] for DW, [k*k*C][Cm] for dense), wp as [Cm][K]
+    std::vector<float> w1t(n_w1), wpt(n_wp);
+    if (dense) {
+        for (int j = 0; j < cm; j++)
+            for (int t = 0; t < k * k; t++)
+                for (int c = 0; c < C; c++)
+                    w1t[((size_t)t * C + c) * cm + j] = host_to_f(hw1.data(), ((size_t)j * k * k + t) * C + c, dt);
+    } else {
+        for (int c = 0; c < C; c++)
+            for (int t = 0; t < k * k; t++)
+                w1t[(size_t)t * C + c] = host_to_f(hw1.data(), (size_t)c * k * k + t, dt);
+    }
+    for (int kk = 0; kk < K; kk++)
+        for (int c = 0; c < cm; c++) wpt[(size_t)c * K + kk] = host_to_f(hwp.data(), (size_t)kk * cm + c, dt);
+
+    if ((st = upload(&h->w1t, w1t.data(), w1t.size())) != FCM_OK ||
+        (st = upload(&h->wpt, wpt.data(), wpt.size())) != FCM_OK ||
+        (st = upload(reinterpret_cast<unsigned char **>(&h->w1_raw), hw1.data(), hw1.size())) != FCM_OK ||
+        (st = upload(&h->s1, reinterpret_cast<const float *>(hs1.data()), cm)) != FCM_OK ||
+        (st = upload(&h->b1, reinterpret_cast<const float *>(hb1.data()), cm)) != FCM_OK ||
+        (st = upload(&h->s2, reinterpret_cast<const float *>(hs2.data()), K)) != FCM_OK ||
+        (st = upload(&h->b2, reinterpret_cast<const float *>(hb2.data()), K)) != FCM_OK) {
+        free_handle(h);
+        return st;
+    }
+    if (h->plan.kernel == FCM_KERNEL_TC) {
+        st = fcm_tc_prepare(h, hw1.data(), hwp.data());
+        if (st != FCM_OK) {
+            free_handle(h);
+            return st;
+        }
+    }
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&h->d_err), sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_handle(h);
+        return cuda_fail(e, "fcm_create");
+    }
+    *out = h;
+    return FCM_OK;
+}
+
+static fcm_status check_ptr(const void *p, const char *name) {
+    if (!p) return fcm_fail(FCM_ERR_INVALID_ARG, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+        return fcm_fail(FCM_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+    return FCM_OK;
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+static fcm_status run_one(fcm_handle *h, int mode, const void *in, void *out, cudaStream_t st) {
+    const bool tc = h->plan.kernel == FCM_KERNEL_TC;
+    const bool dense = h->d.conv1 == FCM_CONV1_DENSE;
+    cudaError_t e = cudaSuccess;
+    switch (mode) {
+    case FCM_MODE_FUSED:
+        e = tc ? (dense ? launch_tc_b2b(h, mode, in, out, st) : launch_tc_dwpw(h, mode, in, out, st))
+               : launch_fused_simt(h, in, out, st);
+        break;
+    case FCM_MODE_CONV1_ONLY:
+        e = tc ? (dense ? launch_tc_b2b(h, mode, in, out, st) : launch_tc_dwpw(h, mode, in, out, st))
+               : launch_conv1_simt(h, in, out, st);
+        break;
+    case FCM_MODE_PW_ONLY:
+        e = tc ? launch_tc_pw(h, in, out, st) : launch_pw_simt(h, in, out, st);
+        break;
+    default: return fcm_fail(FCM_ERR_INVALID_ARG, "mode %d", mode);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return FCM_OK;
+}
+
+fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, void *stream) {
+    if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
+    fcm_status st;
+    if ((st = check_ptr(in, "in")) != FCM_OK || (st = check_ptr(out, "out")) != FCM_OK) return st;
+    if (mode < FCM_MODE_FUSED || mode > FCM_MODE_UNFUSED)
+        return fcm_fail(FCM_ERR_INVALID_ARG, "mode %d", mode);
+    size_t e = h->esize;
+    size_t in_b = (mode == FCM_MODE_PW_ONLY ? h->m_elems : h->x_elems) * e;
+    size_t out_b = (mode == FCM_MODE_CONV1_ONLY ? h->m_elems : h->y_elems) * e;
+    if (overlaps(in, in_b, out, out_b))
+        return fcm_fail(FCM_ERR_INVALID_ARG, "in and out overlap");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == FCM_MODE_UNFUSED) {
+        if (!h->mid_buf) {
+            cudaError_t ce = cudaMalloc(&h->mid_buf, h->m_elems * e);
+            if (ce != cudaSuccess) {
+                h->mid_buf = nullptr;
+                return cuda_fail(ce, "intermediate buffer");
+            }
+            h->mid_bytes = h->m_elems * e;
+        }
+        if ((st = run_one(h, FCM_MODE_CONV1_ONLY, in, h->mid_buf, s)) != FCM_OK) return st;
+        return run_one(h, FCM_MODE_PW_ONLY, h->mid_buf, out, s);
+    }
+    return run_one(h, mode, in, out, s);
+}
+
+fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
+                        void *stream) {
+    if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
+    if (!host_in || !host_out) return fcm_fail(FCM_ERR_INVALID_ARG, "host buffer is NULL");
+    if (mode < FCM_MODE_FUSED || mode > FCM_MODE_UNFUSED)
+        return fcm_fail(FCM_ERR_INVALID_ARG, "mode %d", mode);
+    size_t e = h->esize;
+    size_t in_b = (mode == FCM_MODE_PW_ONLY ? h->m_elems : h->x_elems) * e;
+    size_t out_b = (mode == FCM_MODE_CONV1_ONLY ? h->m_elems : h->y_elems) * e;
+    if (h->stage_in_bytes < in_b) {
+        if (h->stage_in) cudaFree(h->stage_in);
+        h->stage_in = nullptr;
+        h->stage_in_bytes = 0;
+        FCM_CUDA(cudaMalloc(&h->stage_in, in_b));
+        h->stage_in_bytes = in_b;
+    }
+    if (h->stage_out_bytes < out_b) {
+        if (h->stage_out) cudaFree(h->stage_out);
+        h->stage_out = nullptr;
+        h->stage_out_bytes = 0;
+        FCM_CUDA(cudaMalloc(&h->stage_out, out_b));
+        h->stage_out_bytes = out_b;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FCM_CUDA(cudaMemcpyAsync(h->stage_in, host_in, in_b, cudaMemcpyHostToDevice, s));
+    fcm_status st = fcm_run(h, mode, h->stage_in, h->stage_out, stream);
+    if (st != FCM_OK) return st;
+    FCM_CUDA(cudaMemcpyAsync(host_out, h->stage_out, out_b, cudaMemcpyDeviceToHost, s));
+    FCM_CUDA(cudaStreamSynchronize(s));
+    return FCM_OK;
+}
+
+fcm_status fcm_check(fcm_handle *h, void *stream) {
+    if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FCM_CUDA(cudaStreamSynchronize(s));
+    unsigned word = 0;
+    FCM_CUDA(cudaMemcpy(&word, h->d_err, sizeof(word), cudaMemcpyDeviceToHost));
+    if (word) FCM_CUDA(cudaMemset(h->d_err, 0, sizeof(unsigned)));
+    if (word & FCM_DEVERR_TIMEOUT)
+        return fcm_fail(FCM_ERR_TIMEOUT, "a kernel's bounded wait ran out (error word 0x%x)", word);
+    if (word)
+        return fcm_fail(FCM_ERR_DEVICE_FAULT, "a kernel's consistency check failed (error word 0x%x)",
+                        word);
+    return FCM_OK;
+}
+
+void fcm_destroy(fcm_handle *h) {
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_handle(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// fcm_internal.h -- host-side internals shared by the C ABI, the planner and the launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fcm.h"
+
+// Device error word bits, written by kernels with atomicOr and read by fcm_check.
+enum : unsigned {
+    FCM_DEVERR_TIMEOUT = 1u,   // a bounded mbarrier wait gave up
+    FCM_DEVERR_CHECK = 2u,     // a kernel-side consistency check failed
+};
+
+// Planner-chosen configuration of the tensor-core kernels.
+struct TcPlan {
+    int tile_h = 0, tile_w = 0;   // output tile (tile_h * tile_w <= 128 = MMA M)
+    int in_rows = 0, in_cols = 0; // input halo box
+    int chunk_c = 0;              // channels per input stage
+    int nchunks = 0;              // C / chunk_c
+    int stages = 0;               // input ring depth
+    int a_slots = 0;              // A chunk slots (nchunks or 2 * nchunks)
+    int tiles_w = 0, tiles_h = 0; // tiles per image along W and H
+    long long num_tiles = 0;
+    int smem_bytes = 0;
+    int threads = 0;
+    int ctas = 0;
+    int tmem_cols = 0;
+};
+
+struct fcm_handle {
+    fcm_desc d{};
+    fcm_plan_info plan{};
+    TcPlan tc{};
+    int device = -1;
+    int ho = 0, wo = 0, cm = 0;
+    int esize = 0;
+    size_t x_elems = 0, m_elems = 0, y_elems = 0;
+    int num_sms = 0, smem_optin = 0;
+
+    // weights in the layouts the kernels read (all owned, device memory)
+    float *w1t = nullptr;     // DW: [k*k][C] fp32; dense: [k*k*C][Cm] fp32   (SIMT)
+    float *wpt = nullptr;     // [Cm][K] fp32                                  (SIMT)
+    void *w1_raw = nullptr;   // storage dtype, the caller's layout
+    void *wp_img = nullptr;   // tcgen05 B-operand image of wp (128B-swizzled, K-major)
+    size_t wp_img_bytes = 0;
+    void *w1_img = nullptr;   // tcgen05 B-operand images of dense conv1, one per tap
+    size_t w1_img_bytes = 0;
+    float *w1dw_img = nullptr;// DW taps for the tcgen05 DW stage: [C][k*k] fp32
+    float *s1 = nullptr, *b1 = nullptr, *s2 = nullptr, *b2 = nullptr;
+    unsigned *d_err = nullptr;
+
+    void *mid_buf = nullptr;  // FCM_MODE_UNFUSED intermediate (lazily allocated)
+    size_t mid_bytes = 0;
+    void *stage_in = nullptr, *stage_out = nullptr;  // fcm_run_host staging
+    size_t stage_in_bytes = 0, stage_out_bytes = 0;
+};
+
+// thread-local last-error message (fcm_api.cu)
+fcm_status fcm_fail(fcm_status st, const char *fmt, ...);
+
+// planner.cu
+fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm);
+fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm_plan_info *info,
+                         TcPlan *tc);
+int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);
+fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
+                       TcPlan *tc);
+
+// simt_kernels.cu
+cudaError_t launch_conv1_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st);
+cudaError_t launch_pw_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st);
+cudaError_t launch_fused_simt(const fcm_handle *h, const void *x, void *y, cudaStream_t st);
+
+// tc_dwpw.cu (depthwise -> pointwise on tcgen05) and tc_b2b.cu (dense 3x3 -> 1x1)
+cudaError_t launch_tc_dwpw(const fcm_handle *h, int mode, const void *in, void *out,
+                           cudaStream_t st);
+cudaError_t launch_tc_b2b(const fcm_handle *h, int mode, const void *in, void *out,
+                          cudaStream_t st);
+cudaError_t launch_tc_pw(const fcm_handle *h, const void *m, void *y, cudaStream_t st);
+// Build the tcgen05 operand images of the weights (host copies in the caller's layouts).
+fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_host);

@@ -1,0 +1,302 @@
+// simt_kernels.cu -- CUDA-core (SIMT) kernels of the module: the fp32 path and the fallback
+// for shapes the tensor-core kernels do not take.
+//
+//   k_conv1_dw   depthwise k x k + scale/bias/act      -> intermediate in HBM  (LBL DW)
+//   k_conv1_dense dense k x k + scale/bias/act         -> intermediate in HBM  (LBL conv1)
+//   k_pw         1x1 conv + scale/bias/act              (LBL PW)
+//   k_fused      conv1 -> shared-memory commBuffer -> 1x1, one pass (FCM)
+//
+// The fused kernel follows the FCM structure of "Fusing Depthwise and Pointwise Convolutions
+// for Efficient Inference on GPUs", section III-B: the first layer writes its tile of the
+// intermediate, over all channels (section II-D), into a shared buffer, the block
+// synchronizes, and the second layer reads it and writes the output once (output-stationary,
+// section IV-A).  The per-element arithmetic (tap order, fmaf for the norm, rounding of the
+// intermediate to the storage type) is the same in the fused and the layer-by-layer kernels,
+// so fused == conv1-then-PW bit for bit.
+#include <cuda_runtime.h>
+
+#include "fcm_device.cuh"
+#include "fcm_internal.h"
+
+namespace fcm {
+namespace {
+
+constexpr int kPwPixels = 32;      // pixels per CTA in the PW and fused kernels
+constexpr int kThreads = 256;
+
+// Depthwise value for VEC channels c0..c0+VEC-1 of output pixel (n, ho, wo), before the norm.
+template <typename T, int VEC>
+__device__ __forceinline__ void dw_point(const T *__restrict__ x, const float *__restrict__ wt,
+                                         int n, int ho, int wo, int c0, int H, int W, int C,
+                                         int k, int s, int p, float (&acc)[VEC]) {
+#pragma unroll
+    for (int v = 0; v < VEC; v++) acc[v] = 0.0f;
+    for (int i = 0; i < k; i++) {
+        int hi = ho * s - p + i;
+        if (hi < 0 || hi >= H) continue;
+        for (int j = 0; j < k; j++) {
+            int wi = wo * s - p + j;
+            if (wi < 0 || wi >= W) continue;
+            float xv[VEC];
+            load_vec<T, VEC>(x + (((size_t)n * H + hi) * W + wi) * C + c0, xv);
+            const float *wr = wt + (size_t)(i * k + j) * C + c0;
+#pragma unroll
+            for (int v = 0; v < VEC; v++) acc[v] = fmaf(xv[v], __ldg(wr + v), acc[v]);
+        }
+    }
+}
+
+// Dense value for output channel j of pixel (n, ho, wo), before the norm; taps (r, u) then c.
+template <typename T>
+__device__ __forceinline__ float dense_point(const T *__restrict__ x, const float *__restrict__ wt,
+                                             int n, int ho, int wo, int j, int H, int W, int C,
+                                             int Cm, int k, int s, int p) {
+    float acc = 0.0f;
+    for (int r = 0; r < k; r++) {
+        int hi = ho * s - p + r;
+        if (hi < 0 || hi >= H) continue;
+        for (int u = 0; u < k; u++) {
+            int wi = wo * s - p + u;
+            if (wi < 0 || wi >= W) continue;
+            const T *xp = x + (((size_t)n * H + hi) * W + wi) * C;
+            const float *wp = wt + (size_t)((r * k + u) * C) * Cm + j;
+            for (int c = 0; c < C; c++)
+                acc = fmaf(Storage<T>::to_f(xp[c]), __ldg(wp + (size_t)c * Cm), acc);
+        }
+    }
+    return acc;
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kThreads) k_conv1_dw(
+    const T *__restrict__ x, const float *__restrict__ wt, const float *__restrict__ s1,
+    const float *__restrict__ b1, T *__restrict__ m, int N, int H, int W, int C, int Ho, int Wo,
+    int k, int s, int p, int act) {
+    const int cv_per_px = C / VEC;
+    const long long total = (long long)N * Ho * Wo * cv_per_px;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        int cv = (int)(idx % cv_per_px);
+        long long pix = idx / cv_per_px;
+        int wo = (int)(pix % Wo);
+        long long t = pix / Wo;
+        int ho = (int)(t % Ho);
+        int n = (int)(t / Ho);
+        int c0 = cv * VEC;
+        float acc[VEC];
+        dw_point<T, VEC>(x, wt, n, ho, wo, c0, H, W, C, k, s, p, acc);
+#pragma unroll
+        for (int v = 0; v < VEC; v++)
+            acc[v] = act_apply(fmaf(__ldg(s1 + c0 + v), acc[v], __ldg(b1 + c0 + v)), act);
+        store_vec<T, VEC>(m + pix * C + c0, acc);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_conv1_dense(
+    const T *__restrict__ x, const float *__restrict__ wt, const float *__restrict__ s1,
+    const float *__restrict__ b1, T *__restrict__ m, int N, int H, int W, int C, int Cm, int Ho,
+    int Wo, int k, int s, int p, int act) {
+    const long long total = (long long)N * Ho * Wo * Cm;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        int j = (int)(idx % Cm);
+        long long pix = idx / Cm;
+        int wo = (int)(pix % Wo);
+        long long t = pix / Wo;
+        int ho = (int)(t % Ho);
+        int n = (int)(t / Ho);
+        float acc = dense_point<T>(x, wt, n, ho, wo, j, H, W, C, Cm, k, s, p);
+        m[idx] = Storage<T>::from_f(act_apply(fmaf(__ldg(s1 + j), acc, __ldg(b1 + j)), act));
+    }
+}
+
+// 1x1 convolution of a tile of kPwPixels pixels held (as fp32) in shared memory `tile`
+// [kPwPixels][Cm]; thread item = (group of 4 pixels, output channel).
+template <typename T>
+__device__ __forceinline__ void pw_tile(const float *tile, long long p0, long long P, int Cm,
+                                        int K, const float *__restrict__ wpt,
+                                        const float *__restrict__ s2,
+                                        const float *__restrict__ b2, int act, T *__restrict__ y) {
+    const int items = (kPwPixels / 4) * K;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        int kk = it % K;
+        int pg = it / K;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *t0 = tile + (size_t)(pg * 4) * Cm;
+        for (int c = 0; c < Cm; c++) {
+            float w = __ldg(wpt + (size_t)c * K + kk);
+#pragma unroll
+            for (int q = 0; q < 4; q++) acc[q] = fmaf(t0[(size_t)q * Cm + c], w, acc[q]);
+        }
+        float sc = __ldg(s2 + kk), bi = __ldg(b2 + kk);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            long long pix = p0 + pg * 4 + q;
+            if (pix < P) y[pix * K + kk] = Storage<T>::from_f(act_apply(fmaf(sc, acc[q], bi), act));
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_pw(
+    const T *__restrict__ m, const float *__restrict__ wpt, const float *__restrict__ s2,
+    const float *__restrict__ b2, T *__restrict__ y, long long P, int Cm, int K, int act) {
+    extern __shared__ float tile[];   // [kPwPixels][Cm]
+    for (long long blk = blockIdx.x; blk * kPwPixels < P; blk += gridDim.x) {
+        long long p0 = blk * kPwPixels;
+        __syncthreads();
+        for (int e = threadIdx.x; e < kPwPixels * Cm; e += blockDim.x) {
+            long long pix = p0 + e / Cm;
+            tile[e] = pix < P ? Storage<T>::to_f(m[p0 * Cm + e]) : 0.0f;
+        }
+        __syncthreads();
+        pw_tile<T>(tile, p0, P, Cm, K, wpt, s2, b2, act, y);
+    }
+}
+
+// Fused conv1 -> commBuffer -> 1x1.  The commBuffer holds the intermediate of kPwPixels
+// consecutive output pixels over all Cm channels, rounded to the storage type.
+template <typename T, bool DENSE>
+__global__ void __launch_bounds__(kThreads) k_fused(
+    const T *__restrict__ x, const float *__restrict__ w1t, const float *__restrict__ s1,
+    const float *__restrict__ b1, const float *__restrict__ wpt, const float *__restrict__ s2,
+    const float *__restrict__ b2, T *__restrict__ y, int N, int H, int W, int C, int Cm, int K,
+    int Ho, int Wo, int k, int s, int p, int act1, int act2) {
+    extern __shared__ float comm[];   // [kPwPixels][Cm]
+    const long long P = (long long)N * Ho * Wo;
+    for (long long blk = blockIdx.x; blk * kPwPixels < P; blk += gridDim.x) {
+        long long p0 = blk * kPwPixels;
+        __syncthreads();
+        for (int e = threadIdx.x; e < kPwPixels * Cm; e += blockDim.x) {
+            long long pix = p0 + e / Cm;
+            int j = e % Cm;
+            float v = 0.0f;
+            if (pix < P) {
+                int wo = (int)(pix % Wo);
+                long long t = pix / Wo;
+                int ho = (int)(t % Ho);
+                int n = (int)(t / Ho);
+                float acc;
+                if constexpr (DENSE) {
+                    acc = dense_point<T>(x, w1t, n, ho, wo, j, H, W, C, Cm, k, s, p);
+                } else {
+                    float a1[1];
+                    dw_point<T, 1>(x, w1t, n, ho, wo, j, H, W, C, k, s, p, a1);
+                    acc = a1[0];
+                }
+                // round to the storage type exactly as the layer-by-layer path stores it
+                v = Storage<T>::to_f(
+                    Storage<T>::from_f(act_apply(fmaf(__ldg(s1 + j), acc, __ldg(b1 + j)), act1)));
+            }
+            comm[e] = v;
+        }
+        __syncthreads();
+        pw_tile<T>(comm, p0, P, Cm, K, wpt, s2, b2, act2, y);
+    }
+}
+
+int grid_for(long long work_items, int threads, int num_sms) {
+    long long blocks = (work_items + threads - 1) / threads;
+    long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+template <typename T>
+cudaError_t conv1_t(const fcm_handle *h, const void *xin, void *mout, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    const T *x = static_cast<const T *>(xin);
+    T *m = static_cast<T *>(mout);
+    if (d.conv1 == FCM_CONV1_DENSE) {
+        long long items = (long long)d.n * h->ho * h->wo * h->cm;
+        k_conv1_dense<T><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+            x, h->w1t, h->s1, h->b1, m, d.n, d.h, d.w, d.c, h->cm, h->ho, h->wo, d.ksize,
+            d.stride, d.pad, d.act1);
+    } else {
+        constexpr int V16 = 16 / (int)sizeof(T);
+        if (d.c % V16 == 0) {
+            long long items = (long long)d.n * h->ho * h->wo * (d.c / V16);
+            k_conv1_dw<T, V16><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+                x, h->w1t, h->s1, h->b1, m, d.n, d.h, d.w, d.c, h->ho, h->wo, d.ksize, d.stride,
+                d.pad, d.act1);
+        } else {
+            long long items = (long long)d.n * h->ho * h->wo * d.c;
+            k_conv1_dw<T, 1><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+                x, h->w1t, h->s1, h->b1, m, d.n, d.h, d.w, d.c, h->ho, h->wo, d.ksize, d.stride,
+                d.pad, d.act1);
+        }
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t pw_t(const fcm_handle *h, const void *min, void *yout, cudaStream_t st) {
+    long long P = (long long)h->d.n * h->ho * h->wo;
+    size_t smem = sizeof(float) * kPwPixels * h->cm;
+    cudaError_t e = cudaFuncSetAttribute(k_pw<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    long long blocks = (P + kPwPixels - 1) / kPwPixels;
+    int grid = (int)(blocks < (long long)h->num_sms * 8 ? blocks : (long long)h->num_sms * 8);
+    k_pw<T><<<grid, kThreads, smem, st>>>(static_cast<const T *>(min), h->wpt, h->s2, h->b2,
+                                          static_cast<T *>(yout), P, h->cm, h->d.k_out,
+                                          h->d.act2);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t fused_t(const fcm_handle *h, const void *xin, void *yout, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    long long P = (long long)d.n * h->ho * h->wo;
+    size_t smem = sizeof(float) * kPwPixels * h->cm;
+    long long blocks = (P + kPwPixels - 1) / kPwPixels;
+    int grid = (int)(blocks < (long long)h->num_sms * 8 ? blocks : (long long)h->num_sms * 8);
+    cudaError_t e;
+    if (d.conv1 == FCM_CONV1_DENSE) {
+        e = cudaFuncSetAttribute(k_fused<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_fused<T, true><<<grid, kThreads, smem, st>>>(
+            static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
+            static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, d.k_out, h->ho, h->wo, d.ksize,
+            d.stride, d.pad, d.act1, d.act2);
+    } else {
+        e = cudaFuncSetAttribute(k_fused<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_fused<T, false><<<grid, kThreads, smem, st>>>(
+            static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
+            static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, d.k_out, h->ho, h->wo, d.ksize,
+            d.stride, d.pad, d.act1, d.act2);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace fcm
+
+cudaError_t launch_conv1_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st) {
+    switch (h->d.dtype) {
+    case FCM_F32: return fcm::conv1_t<float>(h, x, m, st);
+    case FCM_F16: return fcm::conv1_t<__half>(h, x, m, st);
+    default: return fcm::conv1_t<__nv_bfloat16>(h, x, m, st);
+    }
+}
+
+cudaError_t launch_pw_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st) {
+    switch (h->d.dtype) {
+    case FCM_F32: return fcm::pw_t<float>(h, m, y, st);
+    case FCM_F16: return fcm::pw_t<__half>(h, m, y, st);
+    default: return fcm::pw_t<__nv_bfloat16>(h, m, y, st);
+    }
+}
+
+cudaError_t launch_fused_simt(const fcm_handle *h, const void *x, void *y, cudaStream_t st) {
+    switch (h->d.dtype) {
+    case FCM_F32: return fcm::fused_t<float>(h, x, y, st);
+    case FCM_F16: return fcm::fused_t<__half>(h, x, y, st);
+    default: return fcm::fused_t<__nv_bfloat16>(h, x, y, st);
+    }
+}

@@ -1,0 +1,116 @@
+"""Shared helpers of the GPU tests: storage <-> torch, running a module through the C ABI,
+and the parity bars."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import pointwise_conv_cnn_gb300 as fcm
+from pointwise_conv_cnn_gb300 import workloads as wk
+
+# Parity bars: fp32 max-abs error <= 1e-4 * sqrt(C) with C the 1x1 reduction length;
+# fp16/bf16 max-norm relative error <= 2e-2 (max|gpu - ref| / max|ref|).
+F32_ABS_PER_SQRT_C = 1e-4
+HALF_REL = 2e-2
+
+
+def torch_dtype(dtype: str):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+
+def to_device(arr: np.ndarray, dtype: str, device="cuda"):
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+    return t.to(device)
+
+
+def to_host(t, dtype: str) -> np.ndarray:
+    import torch
+    t = t.detach().cpu()
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16).copy()
+    return t.numpy().copy()
+
+
+def empty(shape, dtype: str, device="cuda", fill=None):
+    import torch
+    t = torch.empty(shape, dtype=torch_dtype(dtype), device=device)
+    if fill is not None:
+        t.fill_(fill)
+    return t
+
+
+def make_module(case: wk.Case, kernel: str = "auto", **desc_over) -> fcm.FusedConvModule:
+    d = fcm.desc_from_workload(case.wl, kernel=kernel, **desc_over)
+    return fcm.FusedConvModule(d, case.w1, case.wp, case.s1, case.b1, case.s2, case.b2)
+
+
+def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
+             module=None):
+    """Run one mode on the GPU; returns (output storage array, module)."""
+    import torch
+    wl = case.wl
+    mod = module or make_module(case, kernel)
+    sh = wl.shapes()
+    x = to_device(case.x if inp is None else inp, wl.dtype)
+    out_shape = sh["m"] if mode == "conv1" else sh["y"]
+    y = empty(out_shape, wl.dtype, fill=float("nan"))
+    mod.run(x, y, mode)
+    torch.cuda.synchronize()
+    mod.check()
+    return to_host(y, wl.dtype), mod
+
+
+def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.ndarray:
+    f = case.f64()
+    wl = case.wl
+    return oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"], wl.act1,
+                        wl.act2, wl.stride, wl.pad, conv1=wl.conv1, mid=mid, nthreads=nthreads)
+
+
+def oracle_conv1(case: wk.Case) -> np.ndarray:
+    f = case.f64()
+    wl = case.wl
+    if wl.conv1 == "dw":
+        return oracle.dw(f["x"], f["w1"], f["s1"], f["b1"], wl.act1, wl.stride, wl.pad)
+    return oracle.dense(f["x"], f["w1"], f["s1"], f["b1"], wl.act1, wl.stride, wl.pad)
+
+
+def oracle_pw(case: wk.Case, m: np.ndarray) -> np.ndarray:
+    f = case.f64()
+    return oracle.pw(m, f["wp"], f["s2"], f["b2"], case.wl.act2)
+
+
+def parity_error(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str) -> float:
+    g = wk.to_f64(gpu_storage, dtype)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), "non-finite output"
+    err = float(np.abs(g - ref).max(initial=0.0))
+    if dtype == "f32":
+        return err
+    return err / max(float(np.abs(ref).max(initial=0.0)), 1e-6)
+
+
+def assert_parity(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str, c_red: int) -> float:
+    e = parity_error(gpu_storage, ref, dtype)
+    bar = F32_ABS_PER_SQRT_C * np.sqrt(c_red) if dtype == "f32" else HALF_REL
+    assert e <= bar, f"parity error {e:.3e} above bar {bar:.3e}"
+    return e
+
+
+def assert_bitexact(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str) -> None:
+    """Exact equality with the oracle rounded once to the storage format (values compared,
+    so +0 and -0 count as equal)."""
+    want = wk.to_f64(wk.to_storage(ref, dtype), dtype)
+    got_f = wk.to_f64(np.asarray(gpu_storage), dtype)
+    got = np.asarray(gpu_storage)
+    eq = got_f == want
+    if not eq.all():
+        idx = np.argwhere(~eq)[:5]
+        raise AssertionError(
+            f"{int((~eq).sum())} of {eq.size} outputs differ; first at {idx.tolist()}: "
+            f"got {[wk.to_f64(got[tuple(i)], dtype) for i in idx]} want {[ref[tuple(i)] for i in idx]}")

@@ -1,0 +1,193 @@
+"""Parity of the CUDA kernels with the fp64 oracle, through the C ABI (needs a GB300).
+
+Bars: bit-exact on integer-valued inputs (index, halo, stride and padding handling); fp32
+max-abs error <= 1e-4*sqrt(C); fp16/bf16 max-norm relative error <= 2e-2.
+"""
+import numpy as np
+import pytest
+
+import pointwise_conv_cnn_gb300 as fcm
+from pointwise_conv_cnn_gb300 import workloads as wk
+
+from helpers import (assert_bitexact, assert_parity, empty, make_module, oracle_conv1,
+                     oracle_fused, oracle_pw, parity_error, run_case, to_device, to_host)
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["simt", "tc"]
+
+
+def reduced(wl: wk.Workload, n=2, hw=None) -> wk.Workload:
+    """Smaller batch (and optionally spatial size) with the layer's own channels, filter,
+    stride, padding, activations and dtype."""
+    kw = {"n": n}
+    if hw is not None:
+        kw.update(h=hw, w=hw)
+    return wl.with_(**kw)
+
+
+def module_or_skip(case, kernel):
+    try:
+        return make_module(case, kernel)
+    except fcm.FcmError as e:
+        if kernel == "tc" and e.status == 2:
+            pytest.skip(f"tensor-core kernels do not take this shape: {e}")
+        raise
+
+
+def integer_variant(wl: wk.Workload) -> wk.Workload:
+    """Shrink the channel count where needed so that the integer case is exact end to end."""
+    if wk.integer_safe(wl):
+        return wl
+    if wl.conv1 == "dense":
+        return wl.with_(c=16, mid=16 if wl.mid else 0)
+    raise AssertionError(wl)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_integer_bitexact_fused_and_unfused(cuda, wl, kernel):
+    small = integer_variant(reduced(wl, n=2, hw=min(wl.h, 30)))
+    case = wk.make_case(small, kind="integer")
+    mod = module_or_skip(case, kernel)
+    ref = oracle_fused(case)
+    for mode in ("fused", "unfused"):
+        got, _ = run_case(case, mode, module=mod)
+        assert_bitexact(got, ref, small.dtype)
+    m_gpu, _ = run_case(case, "conv1", module=mod)
+    assert_bitexact(m_gpu, oracle_conv1(case), small.dtype)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_tolerance_reduced_batch(cuda, wl, kernel):
+    small = reduced(wl, n=2)
+    case = wk.make_case(small)
+    mod = module_or_skip(case, kernel)
+    ref = oracle_fused(case)
+    got, _ = run_case(case, "fused", module=mod)
+    e_f = assert_parity(got, ref, small.dtype, small.cm)
+    got_u, _ = run_case(case, "unfused", module=mod)
+    assert_parity(got_u, ref, small.dtype, small.cm)
+    # the fused and the layer-by-layer path use the same per-element arithmetic
+    assert np.array_equal(wk.to_f64(got, small.dtype), wk.to_f64(got_u, small.dtype)), (
+        "fused and unfused differ", e_f)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_pw_only_on_oracle_intermediate(cuda, wl, kernel):
+    """PW_ONLY on a stored intermediate equals the oracle's 1x1 stage on the same values."""
+    small = reduced(wl, n=1)
+    case = wk.make_case(small)
+    mod = module_or_skip(case, kernel)
+    m_store = wk.to_storage(oracle_conv1(case), small.dtype)
+    ref = oracle_pw(case, wk.to_f64(m_store, small.dtype))
+    import torch
+    y = empty(small.shapes()["y"], small.dtype, fill=float("nan"))
+    mod.run(to_device(m_store, small.dtype), y, "pw")
+    torch.cuda.synchronize()
+    assert_parity(to_host(y, small.dtype), ref, small.dtype, small.cm)
+
+
+EDGE = [  # (N, H, W, C, K, k, s, p, dtype, act1, act2)
+    (1, 1, 1, 16, 16, 3, 1, 1, "f16", "relu", "relu"),
+    (1, 13, 17, 32, 48, 3, 1, 1, "f16", "relu6", "none"),
+    (3, 9, 30, 64, 32, 5, 2, 2, "bf16", "relu", "relu6"),
+    (1, 7, 7, 16, 256, 7, 1, 3, "bf16", "none", "relu"),
+    (2, 11, 5, 48, 16, 1, 1, 0, "f16", "relu", "none"),
+    (1, 20, 131, 16, 16, 3, 1, 1, "f16", "relu", "relu"),
+    (1, 15, 15, 8, 8, 3, 2, 0, "f32", "relu", "relu"),
+    (2, 6, 9, 12, 20, 5, 1, 2, "f32", "relu6", "relu6"),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(map(str, s[:8])) + s[8])
+def test_edge_shapes(cuda, shape, kernel):
+    N, H, W, C, K, k, s, p, dt, a1, a2 = shape
+    wl = wk.Workload("edge", N, H, W, C, K, "dw", k, s, p, a1, a2, dt, "normal")
+    if kernel == "tc" and dt == "f32":
+        pytest.skip("fp32 runs on CUDA cores")
+    case = wk.make_case(wl, seed=77)
+    mod = module_or_skip(case, kernel)
+    got, _ = run_case(case, "fused", module=mod)
+    assert_parity(got, oracle_fused(case), dt, C)
+    icase = wk.make_case(wl, seed=78, kind="integer")
+    if wk.integer_safe(wl):
+        imod = make_module(icase, kernel)
+        got, _ = run_case(icase, "fused", module=imod)
+        assert_bitexact(got, oracle_fused(icase), dt)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_dense_edge_shapes(cuda, kernel):
+    wl = wk.Workload("dense_edge", 2, 9, 13, 32, 48, "dense", 3, 1, 1, "relu", "relu6", "f16",
+                     "normal", mid=32)
+    case = wk.make_case(wl, seed=5)
+    mod = module_or_skip(case, kernel)
+    got, _ = run_case(case, "fused", module=mod)
+    assert_parity(got, oracle_fused(case), "f16", 32)
+
+
+def test_run_host_matches_run(cuda):
+    import torch
+    wl = reduced(wk.BY_NAME["mobilenet_dwpw_f16"], n=2)
+    case = wk.make_case(wl)
+    mod = make_module(case)
+    got, _ = run_case(case, "fused", module=mod)
+    x_h = to_device(case.x, wl.dtype, "cpu").pin_memory()
+    y_h = torch.empty(wl.shapes()["y"], dtype=torch.float16).pin_memory()
+    mod.run_host(x_h, y_h, "fused")
+    assert np.array_equal(y_h.numpy(), got)
+
+
+def test_argument_errors(cuda):
+    import torch
+    wl = reduced(wk.BY_NAME["mobilenet_dwpw_f16"], n=1)
+    case = wk.make_case(wl)
+    mod = make_module(case)
+    x = to_device(case.x, wl.dtype)
+    y = empty(wl.shapes()["y"], wl.dtype)
+    raw = torch.empty(x.numel() * 2 + 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fcm.FcmError) as e:
+        fcm.fcm_run(mod.handle, 0, raw.data_ptr() + 2, y.data_ptr(), 0)
+    assert e.value.status == 3
+    with pytest.raises(fcm.FcmError) as e:
+        fcm.fcm_run(mod.handle, 0, x.data_ptr(), x.data_ptr(), 0)
+    assert e.value.status == 1
+    with pytest.raises(fcm.FcmError) as e:
+        fcm.fcm_run(mod.handle, 9, x.data_ptr(), y.data_ptr(), 0)
+    assert e.value.status == 1
+    mod.check()
+
+
+def test_weights_from_device_memory(cuda):
+    import torch
+    wl = reduced(wk.BY_NAME["stride2_dwpw_bf16"], n=1, hw=20)
+    case = wk.make_case(wl)
+    d = fcm.desc_from_workload(wl)
+    dev = [to_device(a, wl.dtype) for a in (case.w1, case.wp)]
+    sb = [torch.from_numpy(a).cuda() for a in (case.s1, case.b1, case.s2, case.b2)]
+    mod = fcm.FusedConvModule(d, dev[0], dev[1], *sb)
+    got, _ = run_case(case, "fused", module=mod)
+    assert_parity(got, oracle_fused(case), wl.dtype, wl.cm)
+
+
+# ---------------------------------------------------------------- full-size, sampled images
+SAMPLE_IMAGES = 2
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_full_size_sampled(cuda, wl):
+    """The full batch in the launch configuration the benchmark times (planner's choice);
+    the oracle recomputes the first and the last image."""
+    case = wk.make_case(wl)
+    got, mod = run_case(case, "fused")
+    picks = [0, wl.n - 1][:SAMPLE_IMAGES]
+    for i in picks:
+        sub = wk.Case(wl.with_(n=1), case.seed, case.x[i:i + 1], case.w1, case.wp, case.s1,
+                      case.b1, case.s2, case.b2)
+        assert_parity(got[i:i + 1], oracle_fused(sub), wl.dtype, wl.cm)
+    assert np.all(np.isfinite(wk.to_f64(got, wl.dtype)))

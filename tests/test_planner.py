@@ -1,0 +1,98 @@
+"""FusePlanner cost models (section IV, Eq. 1-4) and the tile planner (CPU only)."""
+import numpy as np
+import pytest
+
+import pointwise_conv_cnn_gb300 as fcm
+from oracle import planner_model as pm
+from pointwise_conv_cnn_gb300 import build
+from pointwise_conv_cnn_gb300 import workloads as wk
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return fcm.load_library()
+
+
+def test_eq1_overlap_by_hand():
+    # (ceil(56/28)-1)*(3-1)*56 + (ceil(56/14)-1)*(3-1)*56 = 112 + 336
+    assert pm.overlap(56, 56, 28, 14, 3, 3, 1) == 448
+    assert fcm.fcm_model_overlap(56, 56, 28, 14, 3, 3, 1) == 448
+    # one tile: no overlap
+    assert fcm.fcm_model_overlap(56, 56, 56, 56, 3, 3, 1) == 0
+
+
+def test_eq2_eq3_dwpw_by_hand():
+    # Eq. 2: ceil(100/30)*1000 + 500 + ceil(500/64)*100 = 4000 + 500 + 800
+    assert pm.pw_gma(100, 30, 1000, 500, 64) == 5300
+    assert fcm.fcm_model_pw_gma(100, 30, 1000, 500, 64) == 5300
+    # Eq. 3: 2*8*10 + 1000 + 900 + ceil(100/32)*72 = 160 + 1000 + 900 + 288
+    assert pm.dw_gma(8, 10, 1000, 900, 100, 32, 72) == 2348
+    assert fcm.fcm_model_dw_gma(8, 10, 1000, 900, 100, 32, 72) == 2348
+    # DWPW: (2*8*10 + 1000)*ceil(64/32) + 800 + ceil(100/32)*(72+64) = 2320 + 800 + 544
+    assert pm.dwpw_gma(8, 10, 1000, 64, 32, 800, 100, 32, 72) == 3664
+    assert fcm.fcm_model_dwpw_gma(8, 10, 1000, 64, 32, 800, 100, 32, 72) == 3664
+
+
+def test_eq4_pwdw_as_printed():
+    # (2*16*5 + 400) * max(ceil(64/32), ceil(72/72)) + ceil(300/100)*64 + ceil(50/25)*72
+    #   = 560*2 + 3*64 + 2*72
+    assert pm.pwdw_gma(16, 5, 400, 64, 32, 72, 72, 300, 100, 50, 25) == 1120 + 192 + 144
+
+
+def test_c_models_match_literal_models_randomised():
+    r = np.random.default_rng(0)
+    for _ in range(300):
+        a = [int(v) for v in r.integers(1, 500, 12)]
+        assert fcm.fcm_model_overlap(a[0], a[1], a[2], a[3], a[4] % 7 + 1, a[5] % 7 + 1, a[6] % 2 + 1) == \
+            pm.overlap(a[0], a[1], a[2], a[3], a[4] % 7 + 1, a[5] % 7 + 1, a[6] % 2 + 1)
+        assert fcm.fcm_model_pw_gma(*a[:5]) == pm.pw_gma(*a[:5])
+        assert fcm.fcm_model_dw_gma(*a[:7]) == pm.dw_gma(*a[:7])
+        assert fcm.fcm_model_dwpw_gma(*a[:9]) == pm.dwpw_gma(*a[:9])
+
+
+def test_fig1_fusion_saves_half_of_activation_traffic():
+    """Figure 1 / section I: fusing DW+PW saves 50% of their off-chip accesses (C = K,
+    stride 1, one tile over the image, weights set aside)."""
+    H = W = 56
+    C = K = 128
+    g = pm.layer_pair_gma(H, W, C, K, 3, 1, 1, H, W)
+    weights = C * 9 + K * C
+    lbl = g["lbl"] - weights  # each layer reads its weights once
+    fused = g["fused"] - weights
+    assert g["overlap"] == 0
+    assert fused * 2 == lbl
+
+
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_plan_bytes_match_closed_form(wl):
+    info = fcm.fcm_plan_desc(fcm.desc_from_workload(wl))
+    mb = wl.min_bytes()
+    assert info["bytes_fused_min"] == mb["fused"]
+    assert info["bytes_unfused_min"] == mb["unfused"]
+    assert info["ho"] == wl.ho and info["wo"] == wl.wo
+
+
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_plan_model_matches_literal(wl):
+    if wl.conv1 != "dw":
+        pytest.skip("Eq. 3 models the depthwise layer")
+    info = fcm.fcm_plan_desc(fcm.desc_from_workload(wl))
+    g = pm.layer_pair_gma(wl.h, wl.w, wl.c, wl.k_out, wl.ksize, wl.stride, wl.pad,
+                          info["tile_h"], info["tile_w"])
+    e = wl.esize
+    assert info["overlap_elems"] == g["overlap"]
+    assert info["gma_fused_model"] == g["fused"] * wl.n * e
+    assert info["gma_lbl_model"] == g["lbl"] * wl.n * e
+
+
+def test_fused_saving_closed_forms():
+    """Saving of fusion vs the unfused pair, from the tensor sizes alone: 50% for C=K stride 1
+    (MobileNet), 25% for the stride-2 64->128 layer, 60% for the 240->80 5x5 layer."""
+    expect = {"mobilenet_dwpw_f16": 0.50, "stride2_dwpw_bf16": 0.25, "wide5x5_dwpw_bf16": 0.60,
+              "b2b_dense3x3_f16": 0.50}
+    for name, saving in expect.items():
+        b = wk.BY_NAME[name].min_bytes()
+        io_f = b["x"] + b["y"]
+        io_u = io_f + 2 * b["mid"]
+        assert abs((1 - io_f / io_u) - saving) < 1e-12, name
