@@ -20,7 +20,7 @@ struct TcPlan {
     int chunk_c = 0;              // channels per input stage
     int nchunks = 0;              // C / chunk_c
     int stages = 0;               // input ring depth
-    int a_slots = 0;              // A chunk slots (nchunks or 2 * nchunks)
+    int dw_warps = 0;             // warps running the DW stencil
     int tiles_w = 0, tiles_h = 0; // tiles per image along W and H
     long long num_tiles = 0;
     int smem_bytes = 0;

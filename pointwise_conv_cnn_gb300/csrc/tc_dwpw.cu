@@ -1,0 +1,766 @@
+// tc_dwpw.cu -- the tensor-core (tcgen05) depthwise -> pointwise kernels for sm_103a.
+//
+// One persistent, warp-specialised kernel template serves three modes:
+//   FUSED   halo tile (TMA) -> DW stencil on CUDA cores -> A tile in shared memory ->
+//           1x1 conv as tcgen05.mma into TMEM -> epilogue (scale/bias/act) -> y, stored once
+//   DWONLY  halo tile (TMA) -> DW stencil -> intermediate m in HBM (layer-by-layer baseline)
+//   PWONLY  m tile (TMA, 128B-swizzled) -> tcgen05.mma -> epilogue -> y (layer-by-layer baseline)
+//
+// This is the FCM structure of "Fusing Depthwise and Pointwise Convolutions for Efficient
+// Inference on GPUs" (section III-B: weights prefetched, the first layer's
+// conv-norm-activation written to a shared commBuffer, the second layer reading it and
+// writing the OFMs once), re-designed for Blackwell: the commBuffer IS the A operand of the
+// tensor-core GEMM, written directly in the 128-byte-swizzled K-major layout tcgen05.mma
+// reads (bank-conflict free for the writers, section III-B's concern), and the accumulator
+// lives in tensor memory.  Each output tile covers all channels (section II-D's rule for
+// DWPW), so no block ever needs another block's intermediate.
+//
+// Warp roles (persistent CTA, one per SM, static round-robin over output tiles):
+//   warp 0      TMA producer: input halo tiles (channel chunks) into a ring of stages
+//   warp 1      TMEM owner and MMA issuer (one lane issues)
+//   warps 2-5   epilogue: TMEM -> registers -> scale/bias/act -> global (warp w reads TMEM
+//               lanes 32*(w%4) .. +31)
+//   warps 6..   DW warps: stencil over a stage, result into the A tile (or HBM in DWONLY)
+// Synchronisation is by mbarriers only; every wait is bounded (about one second) and a
+// timeout sets the device error word, raises a CTA-wide abort flag and drains in-flight
+// copies and MMAs before TMEM is released.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "fcm_internal.h"
+#include "tc_common.cuh"
+
+namespace fcm {
+namespace tc {
+
+constexpr int kEpiWarps = 4;
+constexpr int kFirstDwWarp = 2 + kEpiWarps;
+constexpr int kMaxDwWarps = 12;
+constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);
+constexpr int kR = 4;          // output pixels per DW work unit (along W)
+constexpr int kTileM = 128;    // MMA M: pixels per output tile (padded)
+constexpr int kMaxStages = 8;
+constexpr int kMaxChunks = 16;
+
+enum Mode { FUSED = 0, DWONLY = 1, PWONLY = 2 };
+
+struct Args {
+    CUtensorMap tmap;          // x (FUSED/DWONLY: 4-D C,W,H,N) or m (PWONLY: 2-D C,P)
+    void *out;                 // y, or m for DWONLY
+    const uint8_t *wp_img;     // B operand image (K rows, swizzled, K-major)
+    const float *wdw;          // DW taps [C/8][k*k][8]
+    const float *s1, *b1, *s2, *b2;
+    unsigned *err;
+    unsigned long long wait_limit_ns;
+    long long num_tiles;
+    long long P;               // PWONLY: pixel count
+    int N, H, W, C, K, Ho, Wo, pad;
+    int tile_h, tile_w, tiles_w, tiles_per_img, ngroups;
+    int in_rows, in_cols;
+    int chunk_c, nchunks, stages, n_dw_warps;
+    int act1, act2;
+    uint32_t tmem_cols, idesc, wp_img_bytes, in_stage_bytes, a_bytes;
+    uint32_t off_b, off_a, off_in, in_stage_stride, off_wdw, off_sb, off_bar;
+};
+
+struct Bars {
+    uint32_t full, empty, afull, aempty, accfull, accempty, wbar, drain;
+    __device__ Bars(uint32_t base) {
+        full = base;
+        empty = full + 8 * kMaxStages;
+        afull = empty + 8 * kMaxStages;
+        aempty = afull + 8 * kMaxChunks;
+        accfull = aempty + 8 * kMaxChunks;
+        accempty = accfull + 16;
+        wbar = accempty + 16;
+        drain = wbar + 8;
+    }
+};
+constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 2 * kMaxChunks + 4 + 2) + 16;
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8]) {
+    const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = Storage<T>::to_f(e[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint4 u;
+    T *e = reinterpret_cast<T *>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; i++) e[i] = Storage<T>::from_f(v[i]);
+    return u;
+}
+
+// One DW work unit: kR consecutive output pixels of one tile row, 8 channels.
+template <typename T, int KS, int S, int MODE>
+__device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_t stage_saddr,
+                                        const float *wdw_s, const float *s1_s, const float *b1_s,
+                                        uint32_t a_saddr, int n, int ho0, int wo0) {
+    const int nv = a.chunk_c >> 3;
+    const int v = u % nv;
+    const int rest = u / nv;
+    const int g = rest % a.ngroups;
+    const int r = rest / a.ngroups;
+    const int oc0 = g * kR;
+    const int c_glob = chunk * a.chunk_c + v * 8;
+    const uint32_t row_bytes = (uint32_t)a.in_cols * a.chunk_c * 2;
+    const uint32_t px_bytes = (uint32_t)a.chunk_c * 2;
+
+    float acc[kR][8];
+#pragma unroll
+    for (int jj = 0; jj < kR; jj++)
+#pragma unroll
+        for (int c = 0; c < 8; c++) acc[jj][c] = 0.0f;
+
+    const float4 *wv = reinterpret_cast<const float4 *>(wdw_s) + (size_t)(c_glob >> 3) * KS * KS * 2;
+#pragma unroll
+    for (int i = 0; i < KS; i++) {
+        float w[KS][8];
+#pragma unroll
+        for (int t = 0; t < KS; t++) {
+            float4 lo = wv[(i * KS + t) * 2], hi = wv[(i * KS + t) * 2 + 1];
+            w[t][0] = lo.x; w[t][1] = lo.y; w[t][2] = lo.z; w[t][3] = lo.w;
+            w[t][4] = hi.x; w[t][5] = hi.y; w[t][6] = hi.z; w[t][7] = hi.w;
+        }
+        const uint32_t rbase = stage_saddr + (uint32_t)(r * S + i) * row_bytes +
+                               (uint32_t)(oc0 * S) * px_bytes + (uint32_t)v * 16;
+#pragma unroll
+        for (int q = 0; q < (kR - 1) * S + KS; q++) {
+            uint4 raw;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                         : "r"(rbase + (uint32_t)q * px_bytes));
+            float xv[8];
+            unpack8<T>(raw, xv);
+#pragma unroll
+            for (int jj = 0; jj < kR; jj++) {
+                const int t = q - jj * S;
+                if (t >= 0 && t < KS) {
+#pragma unroll
+                    for (int c = 0; c < 8; c++) acc[jj][c] = fmaf(xv[c], w[t][c], acc[jj][c]);
+                }
+            }
+        }
+    }
+    float sc[8], bi[8];
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        sc[c] = s1_s[c_glob + c];
+        bi[c] = b1_s[c_glob + c];
+    }
+#pragma unroll
+    for (int jj = 0; jj < kR; jj++) {
+        const int oc = oc0 + jj;
+        if (oc >= a.tile_w) break;
+        float o[8];
+#pragma unroll
+        for (int c = 0; c < 8; c++) o[c] = act_apply(fmaf(sc[c], acc[jj][c], bi[c]), a.act1);
+        uint4 packed = pack8<T>(o);
+        if (MODE == FUSED) {
+            const int m_row = r * a.tile_w + oc;
+            const uint32_t off = sw128_offset(m_row, c_glob, kTileM, 2);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a_saddr + off),
+                         "r"(packed.x), "r"(packed.y), "r"(packed.z), "r"(packed.w)
+                         : "memory");
+        } else {
+            const int ho = ho0 + r, wo = wo0 + oc;
+            if (ho < a.Ho && wo < a.Wo) {
+                T *dst = static_cast<T *>(a.out) +
+                         (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
+                *reinterpret_cast<uint4 *>(dst) = packed;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const Args &a, long long t, int &n, int &ho0,
+                                            int &wo0) {
+    n = (int)(t / a.tiles_per_img);
+    int rem = (int)(t % a.tiles_per_img);
+    ho0 = (rem / a.tiles_w) * a.tile_h;
+    wo0 = (rem % a.tiles_w) * a.tile_w;
+}
+
+template <typename T, int KS, int S, int MODE>
+__global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_constant__ Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base_g = smem_raw + (base_s - raw_s);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool has_mma = MODE != DWONLY;
+    const bool has_dw = MODE != PWONLY;
+
+    float *wdw_s = reinterpret_cast<float *>(base_g + a.off_wdw);
+    float *sb_s = reinterpret_cast<float *>(base_g + a.off_sb);
+    float *s1_s = sb_s, *b1_s = sb_s + a.C, *s2_s = sb_s + 2 * a.C, *b2_s = sb_s + 2 * a.C + a.K;
+    const uint32_t bar_base = base_s + a.off_bar;
+    Bars bars(bar_base);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base_g + a.off_bar + kBarBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base_g + a.off_bar + kBarBytes + 4);
+
+    // ---- prologue: weights/scales to shared memory, barriers, TMEM
+    if (has_dw) {
+        const int nw = a.C * KS * KS;
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) wdw_s[i] = a.wdw[i];
+    }
+    for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
+        s1_s[i] = a.s1[i];
+        b1_s[i] = a.b1[i];
+    }
+    for (int i = threadIdx.x; i < a.K; i += blockDim.x) {
+        s2_s[i] = a.s2[i];
+        b2_s[i] = a.b2[i];
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; s++) {
+            mbar_init(bars.full + 8 * s, 1);
+            mbar_init(bars.empty + 8 * s, MODE == PWONLY ? 1 : a.n_dw_warps);
+        }
+        if (MODE == FUSED) {
+            for (int j = 0; j < a.nchunks; j++) {
+                mbar_init(bars.afull + 8 * j, a.n_dw_warps);
+                mbar_init(bars.aempty + 8 * j, 1);
+            }
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(bars.accfull + 8 * b, 1);
+            mbar_init(bars.accempty + 8 * b, kEpiWarps);
+        }
+        mbar_init(bars.wbar, 1);
+        mbar_init(bars.drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (has_mma && warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), a.tmem_cols);
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = has_mma ? *tmem_slot : 0u;
+    const unsigned long long lim = a.wait_limit_ns;
+
+    if (warp == 0) {
+        // ===================================================== TMA producer
+        int issued_per_stage[kMaxStages];
+        for (int s = 0; s < kMaxStages; s++) issued_per_stage[s] = 0;
+        bool ok = true;
+        if (has_mma && lane == 0) {
+            mbar_arrive_expect_tx(bars.wbar, a.wp_img_bytes);
+            bulk_load(base_s + a.off_b, a.wp_img, a.wp_img_bytes, bars.wbar);
+        }
+        if (lane == 0) tma_prefetch_desc(&a.tmap);
+        int it = 0;
+        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
+            int n = 0, ho0 = 0, wo0 = 0;
+            if (MODE != PWONLY) tile_coords(a, t, n, ho0, wo0);
+            const int nloads = MODE == PWONLY ? 1 : a.nchunks;
+            for (int j = 0; j < nloads; j++, it++) {
+                const int s = it % a.stages;
+                const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+                if (!mbar_wait(bars.empty + 8 * s, ph ^ 1u, abort_flag, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t dst = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
+                    mbar_arrive_expect_tx(bars.full + 8 * s, a.in_stage_bytes);
+                    if (MODE == PWONLY) {
+                        const int nkb = (a.C + 63) / 64;
+                        for (int kb = 0; kb < nkb; kb++)
+                            tma_load_2d(dst + (uint32_t)kb * kTileM * 128, &a.tmap, bars.full + 8 * s,
+                                        kb * 64, (int)(t * kTileM));
+                    } else {
+                        tma_load_4d(dst, &a.tmap, bars.full + 8 * s, j * a.chunk_c,
+                                    wo0 * S - a.pad, ho0 * S - a.pad, n);
+                    }
+                }
+                issued_per_stage[s]++;
+                __syncwarp();
+            }
+        }
+        if (!ok) {
+            // drain: every copy this warp issued lands before the CTA exits
+            volatile int no_abort = 0;
+            for (int s = 0; s < a.stages; s++)
+                if (issued_per_stage[s] > 0)
+                    mbar_wait(bars.full + 8 * s, (uint32_t)(issued_per_stage[s] - 1) & 1u,
+                              &no_abort, a.err, lim);
+            if (has_mma) mbar_wait(bars.wbar, 0, &no_abort, a.err, lim);
+        }
+    } else if (warp == 1 && has_mma) {
+        // ===================================================== MMA issuer
+        bool ok = mbar_wait(bars.wbar, 0, abort_flag, a.err, lim);
+        const uint32_t b_s = base_s + a.off_b;
+        const int kb_rows_b = a.K;   // rows of each 64-wide K block of B
+        int lt = 0, it = 0;
+        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
+            const int ab = lt & 1;
+            if (!mbar_wait(bars.accempty + 8 * ab, ((uint32_t)(lt >> 1) & 1u) ^ 1u, abort_flag,
+                           a.err, lim)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)ab * (a.tmem_cols >> 1);
+            if (MODE == PWONLY) {
+                const int s = it % a.stages;
+                const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+                it++;
+                if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
+                if (lane == 0) {
+                    for (int k16 = 0; k16 < a.C / 16; k16++) {
+                        const uint32_t koff = (uint32_t)(k16 & 3) * 32u;
+                        const uint64_t ad = sw128_kmajor_desc(a_s + (uint32_t)(k16 >> 2) * kTileM * 128 + koff);
+                        const uint64_t bd = sw128_kmajor_desc(b_s + (uint32_t)(k16 >> 2) * kb_rows_b * 128 + koff);
+                        mma_f16(d_tmem, ad, bd, a.idesc, k16 > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bars.empty + 8 * s);
+                    mma_commit(bars.accfull + 8 * ab);
+                }
+                __syncwarp();
+            } else {
+                const uint32_t a_s = base_s + a.off_a;
+                const int k16_per_chunk = a.chunk_c / 16;
+                for (int j = 0; j < a.nchunks; j++) {
+                    if (!mbar_wait(bars.afull + 8 * j, (uint32_t)lt & 1u, abort_flag, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        for (int kk = 0; kk < k16_per_chunk; kk++) {
+                            const int k16 = j * k16_per_chunk + kk;
+                            const uint32_t koff = (uint32_t)(k16 & 3) * 32u;
+                            const uint64_t ad = sw128_kmajor_desc(a_s + (uint32_t)(k16 >> 2) * kTileM * 128 + koff);
+                            const uint64_t bd = sw128_kmajor_desc(b_s + (uint32_t)(k16 >> 2) * kb_rows_b * 128 + koff);
+                            mma_f16(d_tmem, ad, bd, a.idesc, k16 > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bars.aempty + 8 * j);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(bars.accfull + 8 * ab);
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            volatile int no_abort = 0;
+            mma_commit(bars.drain);
+            mbar_wait(bars.drain, 0, &no_abort, a.err, lim);
+        }
+        __syncwarp();
+    } else if (warp >= 2 && warp < 2 + kEpiWarps && has_mma) {
+        // ===================================================== epilogue
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int lt = 0;
+        T *y = static_cast<T *>(a.out);
+        for (long long t = blockIdx.x; t < a.num_tiles; t += gridDim.x, lt++) {
+            const int ab = lt & 1;
+            if (!mbar_wait(bars.accfull + 8 * ab, (uint32_t)(lt >> 1) & 1u, abort_flag, a.err, lim))
+                break;
+            tc_fence_after();
+            long long pix = -1;
+            if (MODE == PWONLY) {
+                long long p = t * kTileM + row;
+                if (p < a.P) pix = p;
+            } else {
+                int n, ho0, wo0;
+                tile_coords(a, t, n, ho0, wo0);
+                const int r = row / a.tile_w, oc = row % a.tile_w;
+                if (row < a.tile_h * a.tile_w && ho0 + r < a.Ho && wo0 + oc < a.Wo)
+                    pix = ((long long)n * a.Ho + ho0 + r) * a.Wo + wo0 + oc;
+            }
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
+            for (int c0 = 0; c0 < a.K; c0 += 16) {
+                uint32_t rr[16];
+                tmem_ld16(taddr + (uint32_t)c0, rr);
+                tmem_ld_wait();
+                if (pix >= 0) {
+                    float o[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        o[i] = act_apply(fmaf(s2_s[c0 + i], __uint_as_float(rr[i]), b2_s[c0 + i]), a.act2);
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        lo[i] = o[i];
+                        hi[i] = o[8 + i];
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(y + pix * a.K + c0);
+                    dst[0] = pack8<T>(lo);
+                    dst[1] = pack8<T>(hi);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.accempty + 8 * ab);
+        }
+    } else if (warp >= kFirstDwWarp && has_dw) {
+        // ===================================================== DW warps
+        const int tid = (warp - kFirstDwWarp) * 32 + lane;
+        const int nthr = a.n_dw_warps * 32;
+        const int units = a.tile_h * a.ngroups * (a.chunk_c >> 3);
+        const uint32_t a_s = base_s + a.off_a;
+        int lt = 0, it = 0;
+        bool ok = true;
+        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
+            int n, ho0, wo0;
+            tile_coords(a, t, n, ho0, wo0);
+            for (int j = 0; j < a.nchunks; j++, it++) {
+                const int s = it % a.stages;
+                const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+                if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                if (MODE == FUSED &&
+                    !mbar_wait(bars.aempty + 8 * j, ((uint32_t)lt & 1u) ^ 1u, abort_flag, a.err, lim)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t stage_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
+                for (int u = tid; u < units; u += nthr)
+                    dw_unit<T, KS, S, MODE>(a, u, j, stage_s, wdw_s, s1_s, b1_s, a_s, n, ho0, wo0);
+                if (MODE == FUSED) fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bars.empty + 8 * s);
+                    if (MODE == FUSED) mbar_arrive(bars.afull + 8 * j);
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    __syncthreads();
+    if (has_mma && warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, a.tmem_cols);
+    }
+}
+
+// ================================================================================== host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+uint32_t pow2_cols(int k2) {
+    uint32_t c = 32;
+    while ((int)c < k2) c <<= 1;
+    return c;
+}
+
+// Shared-memory layout of one mode for a plan.  Returns total bytes (incl. alignment slack).
+struct Layout {
+    uint32_t off_b, off_a, off_in, in_stage_bytes, in_stage_stride, off_wdw, off_sb, off_bar,
+        total;
+    int stages;
+};
+
+Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int smem_cap) {
+    Layout L{};
+    const int C = cm, K = d->k_out, nkb = (C + 63) / 64;
+    const uint32_t b_bytes = mode == DWONLY ? 0u : (uint32_t)nkb * K * 128;
+    const uint32_t a_bytes = mode == FUSED ? (uint32_t)nkb * kTileM * 128 : 0u;
+    L.off_b = 0;
+    L.off_a = align_up(b_bytes, 1024);
+    L.off_in = align_up(L.off_a + a_bytes, 1024);
+    if (mode == PWONLY)
+        L.in_stage_bytes = (uint32_t)nkb * kTileM * 128;
+    else
+        L.in_stage_bytes = (uint32_t)p.in_rows * p.in_cols * p.chunk_c * 2;
+    L.in_stage_stride = align_up(L.in_stage_bytes, 1024);
+    const uint32_t wdw = mode == PWONLY ? 0u : (uint32_t)C * d->ksize * d->ksize * 4;
+    const uint32_t sb = (uint32_t)(2 * C + 2 * K) * 4;
+    const uint32_t tail = align_up(wdw, 16) + align_up(sb, 16) + kBarBytes + 16 + 1024;
+    int stages = mode == PWONLY ? 4 : p.stages;
+    for (; stages >= 1; stages--) {
+        uint32_t total = L.off_in + (uint32_t)stages * L.in_stage_stride + tail;
+        if ((int)total <= smem_cap) break;
+    }
+    if (stages > kMaxStages) stages = kMaxStages;
+    L.stages = stages;
+    L.off_wdw = L.off_in + (uint32_t)std::max(stages, 0) * L.in_stage_stride;
+    L.off_sb = L.off_wdw + align_up(wdw, 16);
+    L.off_bar = L.off_sb + align_up(sb, 16);
+    L.total = L.off_bar + kBarBytes + 16 + 1024;
+    return L;
+}
+
+}  // namespace tc
+}  // namespace fcm
+
+using namespace fcm::tc;
+
+int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why) {
+    auto no = [&](const char *w) {
+        if (why) *why = w;
+        return 0;
+    };
+    if (d->dtype == FCM_F32) return no("fp32 runs on CUDA cores");
+    if (d->conv1 != FCM_CONV1_DEPTHWISE) return no("dense conv1 is not on tensor cores yet");
+    if (cm % 16 != 0) return no("channels must be a multiple of 16");
+    if (d->k_out % 16 != 0 || d->k_out < 16 || d->k_out > 256)
+        return no("k_out must be a multiple of 16 in [16, 256]");
+    if (d->ksize != 1 && d->ksize != 3 && d->ksize != 5 && d->ksize != 7)
+        return no("ksize must be 1, 3, 5 or 7");
+    (void)ho;
+    (void)wo;
+    return 1;
+}
+
+fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_cap,
+                       TcPlan *p) {
+    const int S = d->stride, KS = d->ksize, C = cm;
+    TcPlan best;
+    double best_score = -1.0;
+    int tw_choices[2] = {0, 0};
+    int ncol_tiles = (wo + kTileM - 1) / kTileM;
+    tw_choices[0] = (wo + ncol_tiles - 1) / ncol_tiles;
+    if (d->tile_w > 0) tw_choices[0] = std::min(d->tile_w, kTileM);
+    for (int tw : tw_choices) {
+        if (tw <= 0) continue;
+        int ngroups = (tw + kR - 1) / kR;
+        int in_cols = (ngroups * kR - 1) * S + KS;
+        if (in_cols > 256) continue;
+        int th_max = std::max(1, std::min(kTileM / tw, ho));
+        for (int th = th_max; th >= 1; th--) {
+            if (d->tile_h > 0 && th != d->tile_h) continue;
+            int in_rows = (th - 1) * S + KS;
+            if (in_rows > 256) continue;
+            for (int chunk = std::min(C, 256); chunk >= 16; chunk -= 16) {
+                if (C % chunk != 0 || C / chunk > kMaxChunks) continue;
+                TcPlan t;
+                t.tile_h = th;
+                t.tile_w = tw;
+                t.in_rows = in_rows;
+                t.in_cols = in_cols;
+                t.chunk_c = chunk;
+                t.nchunks = C / chunk;
+                t.stages = kMaxStages;
+                Layout L = make_layout(d, t, cm, FUSED, smem_cap);
+                if (L.stages < 2) continue;
+                t.stages = L.stages;
+                t.smem_bytes = (int)L.total;
+                t.tiles_w = (wo + tw - 1) / tw;
+                t.tiles_h = (ho + th - 1) / th;
+                t.num_tiles = (long long)d->n * t.tiles_w * t.tiles_h;
+                // DW warps: best use of threads for this chunk's work units
+                int units = th * ngroups * (chunk / 8);
+                int best_w = 4;
+                double best_eff = 0.0;
+                for (int w = 4; w <= kMaxDwWarps; w++) {
+                    int thr = 32 * w;
+                    double eff = (double)units / ((double)((units + thr - 1) / thr) * thr);
+                    if (eff > best_eff + 1e-9 || (eff > best_eff - 1e-9 && w > best_w)) {
+                        best_eff = eff;
+                        best_w = w;
+                    }
+                }
+                t.threads = 32 * (kFirstDwWarp + best_w);
+                t.dw_warps = best_w;
+                t.ctas = (int)std::min<long long>(t.num_tiles, num_sms);
+                t.tmem_cols = (int)pow2_cols(2 * d->k_out);
+                // score: pixels per tile (MMA/halo efficiency) x thread efficiency x pipeline
+                double halo = (double)(th * tw * S * S) / (double)(in_rows * in_cols);
+                double score = (double)(th * tw) / kTileM * best_eff * (0.5 + 0.5 * halo) *
+                               (t.stages >= 3 ? 1.0 : 0.9) *
+                               (t.num_tiles >= num_sms ? 1.0 : 0.5);
+                if (score > best_score + 1e-12) {
+                    best_score = score;
+                    best = t;
+                }
+            }
+        }
+    }
+    if (best_score < 0) return FCM_ERR_SMEM_BUDGET;
+    *p = best;
+    return FCM_OK;
+}
+
+fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_host) {
+    const fcm_desc &d = h->d;
+    const int C = h->cm, K = d.k_out, KS = d.ksize, nkb = (C + 63) / 64;
+    // B operand image: row n = output channel, K-dim = input channel, 128B swizzle
+    h->wp_img_bytes = (size_t)nkb * K * 128;
+    std::vector<uint8_t> img(h->wp_img_bytes, 0);
+    const uint16_t *wp16 = static_cast<const uint16_t *>(wp_host);
+    for (int n = 0; n < K; n++)
+        for (int c = 0; c < C; c++) {
+            uint32_t off = sw128_offset(n, c, K, 2);
+            memcpy(&img[off], &wp16[(size_t)n * C + c], 2);
+        }
+    // DW taps as fp32 [C/8][k*k][8]
+    std::vector<float> wdw((size_t)C * KS * KS);
+    for (int c = 0; c < C; c++)
+        for (int t = 0; t < KS * KS; t++) {
+            float v;
+            uint16_t bits = static_cast<const uint16_t *>(w1_host)[(size_t)c * KS * KS + t];
+            if (d.dtype == FCM_F16) {
+                __half hv;
+                memcpy(&hv, &bits, 2);
+                v = __half2float(hv);
+            } else {
+                uint32_t u = (uint32_t)bits << 16;
+                memcpy(&v, &u, 4);
+            }
+            wdw[((size_t)(c / 8) * KS * KS + t) * 8 + (c % 8)] = v;
+        }
+    if (cudaMalloc(&h->wp_img, h->wp_img_bytes) != cudaSuccess ||
+        cudaMemcpy(h->wp_img, img.data(), h->wp_img_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(reinterpret_cast<void **>(&h->w1dw_img), wdw.size() * 4) != cudaSuccess ||
+        cudaMemcpy(h->w1dw_img, wdw.data(), wdw.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        return fcm_fail(FCM_ERR_CUDA, "tensor-core weight images: %s",
+                        cudaGetErrorString(cudaGetLastError()));
+    return FCM_OK;
+}
+
+namespace {
+
+template <typename T, int KS, int S, int MODE>
+cudaError_t launch_t(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
+    auto k = dwpw_kernel<T, KS, S, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<ctas, threads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int MODE>
+cudaError_t dispatch_ks(const Args &a, int ks, int s, int ctas, int threads, uint32_t smem,
+                        cudaStream_t st) {
+    if (MODE == PWONLY) return launch_t<T, 1, 1, MODE>(a, ctas, threads, smem, st);
+#define FCM_CASE(KSV, SV) \
+    if (ks == KSV && s == SV) return launch_t<T, KSV, SV, MODE>(a, ctas, threads, smem, st);
+    FCM_CASE(1, 1) FCM_CASE(1, 2) FCM_CASE(3, 1) FCM_CASE(3, 2)
+    FCM_CASE(5, 1) FCM_CASE(5, 2) FCM_CASE(7, 1) FCM_CASE(7, 2)
+#undef FCM_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    const TcPlan &p = h->tc;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    Layout L = make_layout(&d, p, h->cm, mode, h->smem_optin);
+    if (L.stages < 1) return cudaErrorInvalidConfiguration;
+    Args a;
+    memset(&a, 0, sizeof(a));
+    const CUtensorMapDataType dt =
+        d.dtype == FCM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult cr;
+    if (mode == PWONLY) {
+        long long P = (long long)d.n * h->ho * h->wo;
+        cuuint64_t gdim[2] = {(cuuint64_t)h->cm, (cuuint64_t)P};
+        cuuint64_t gstride[1] = {(cuuint64_t)h->cm * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kTileM};
+        cuuint32_t estr[2] = {1, 1};
+        cr = enc(&a.tmap, dt, 2, const_cast<void *>(in), gdim, gstride, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        a.P = P;
+        a.num_tiles = (P + kTileM - 1) / kTileM;
+    } else {
+        cuuint64_t gdim[4] = {(cuuint64_t)d.c, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
+        cuuint64_t gstride[3] = {(cuuint64_t)d.c * 2, (cuuint64_t)d.w * d.c * 2,
+                                 (cuuint64_t)d.h * d.w * d.c * 2};
+        cuuint32_t box[4] = {(cuuint32_t)p.chunk_c, (cuuint32_t)p.in_cols, (cuuint32_t)p.in_rows, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        cr = enc(&a.tmap, dt, 4, const_cast<void *>(in), gdim, gstride, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        a.num_tiles = p.num_tiles;
+    }
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    a.out = out;
+    a.wp_img = static_cast<const uint8_t *>(h->wp_img);
+    a.wdw = h->w1dw_img;
+    a.s1 = h->s1;
+    a.b1 = h->b1;
+    a.s2 = h->s2;
+    a.b2 = h->b2;
+    a.err = h->d_err;
+    a.wait_limit_ns = kWaitLimitNs;
+    a.N = d.n; a.H = d.h; a.W = d.w; a.C = h->cm; a.K = d.k_out; a.Ho = h->ho; a.Wo = h->wo;
+    a.pad = d.pad;
+    a.tile_h = p.tile_h;
+    a.tile_w = p.tile_w;
+    a.tiles_w = p.tiles_w;
+    a.tiles_per_img = p.tiles_w * p.tiles_h;
+    a.ngroups = (p.tile_w + kR - 1) / kR;
+    a.in_rows = p.in_rows;
+    a.in_cols = p.in_cols;
+    a.chunk_c = p.chunk_c;
+    a.nchunks = p.nchunks;
+    a.stages = L.stages;
+    a.n_dw_warps = mode == PWONLY ? 0 : p.dw_warps;
+    a.act1 = d.act1;
+    a.act2 = d.act2;
+    a.tmem_cols = (uint32_t)p.tmem_cols;
+    a.idesc = idesc_f16(d.dtype == FCM_BF16, kTileM, d.k_out);
+    a.wp_img_bytes = (uint32_t)h->wp_img_bytes;
+    a.in_stage_bytes = L.in_stage_bytes;
+    a.in_stage_stride = L.in_stage_stride;
+    a.off_b = L.off_b;
+    a.off_a = L.off_a;
+    a.off_in = L.off_in;
+    a.off_wdw = L.off_wdw;
+    a.off_sb = L.off_sb;
+    a.off_bar = L.off_bar;
+    const int threads = mode == PWONLY ? 32 * kFirstDwWarp : p.threads;
+    const int ctas = (int)std::min<long long>(a.num_tiles, h->num_sms);
+    if (d.dtype == FCM_F16) {
+        if (mode == FUSED) return dispatch_ks<__half, FUSED>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+        if (mode == DWONLY) return dispatch_ks<__half, DWONLY>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+        return dispatch_ks<__half, PWONLY>(a, 1, 1, ctas, threads, L.total, st);
+    }
+    if (mode == FUSED) return dispatch_ks<__nv_bfloat16, FUSED>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+    if (mode == DWONLY) return dispatch_ks<__nv_bfloat16, DWONLY>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+    return dispatch_ks<__nv_bfloat16, PWONLY>(a, 1, 1, ctas, threads, L.total, st);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_dwpw(const fcm_handle *h, int mode, const void *in, void *out,
+                           cudaStream_t st) {
+    return launch_mode(h, mode == FCM_MODE_FUSED ? FUSED : DWONLY, in, out, st);
+}
+
+cudaError_t launch_tc_pw(const fcm_handle *h, const void *m, void *y, cudaStream_t st) {
+    return launch_mode(h, PWONLY, m, y, st);
+}
