@@ -47,7 +47,7 @@ struct fcm_handle {
     size_t wp_img_bytes = 0;
     void *w1_img = nullptr;   // tcgen05 B-operand images of dense conv1, one per tap
     size_t w1_img_bytes = 0;
-    float *w1dw_img = nullptr;// DW taps for the tcgen05 DW stage: [C][k*k] fp32
+    void *w1dw_img = nullptr; // DW taps for the tcgen05 DW stage: [k*k][C], storage dtype
     float *s1 = nullptr, *b1 = nullptr, *s2 = nullptr, *b2 = nullptr;
     unsigned *d_err = nullptr;
 

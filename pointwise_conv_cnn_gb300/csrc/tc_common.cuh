@@ -112,6 +112,102 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// Tensor stores shared -> global (bulk async-group completion; out-of-range box parts are
+// clipped by the TMA unit).
+__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N committed bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Barrier among `nthreads` threads (a multiple of 32) on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier among `nthreads` threads on barrier `id` that also returns the OR of `pred` over
+// them, so that every participant takes the same branch afterwards.
+__device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------- mixed-precision multiply-add
+// acc0 += lo(x2) * lo(w2), acc1 += hi(x2) * hi(w2): 16-bit inputs, exact products, fp32 sum
+// rounded once (the same result as widening both inputs to fp32 and using fmaf).
+template <typename T> struct Fma16;
+template <> struct Fma16<__half> {
+    static __device__ __forceinline__ void fma2(float &acc0, float &acc1, uint32_t x2, uint32_t w2) {
+        asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+            "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, xl, wl, %0;\n\tfma.rn.f32.f16 %1, xh, wh, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1)
+            : "r"(x2), "r"(w2));
+    }
+};
+template <> struct Fma16<__nv_bfloat16> {
+    static __device__ __forceinline__ void fma2(float &acc0, float &acc1, uint32_t x2, uint32_t w2) {
+        asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+            "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, xl, wl, %0;\n\tfma.rn.f32.bf16 %1, xh, wh, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1)
+            : "r"(x2), "r"(w2));
+    }
+};
+
+// Round two fp32 values to a packed 16-bit pair (round to nearest even), then apply the
+// activation on the pair.  Clamping after rounding equals rounding after clamping because
+// rounding is monotonic and 0 and 6 are exact.
+template <typename T> struct Pack2;
+template <> struct Pack2<__half> {
+    static __device__ __forceinline__ uint32_t run(float a, float b, int act) {
+        __half2 h = __floats2half2_rn(a, b);
+        if (act != 0) h = __hmax2(h, __float2half2_rn(0.0f));
+        if (act == 2) h = __hmin2(h, __float2half2_rn(6.0f));
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+template <> struct Pack2<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t run(float a, float b, int act) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        if (act != 0) h = __hmax2(h, __float2bfloat162_rn(0.0f));
+        if (act == 2) h = __hmin2(h, __float2bfloat162_rn(6.0f));
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
 // -------------------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),

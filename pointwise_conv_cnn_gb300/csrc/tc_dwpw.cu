@@ -50,9 +50,10 @@ enum Mode { FUSED = 0, DWONLY = 1, PWONLY = 2 };
 
 struct Args {
     CUtensorMap tmap;          // x (FUSED/DWONLY: 4-D C,W,H,N) or m (PWONLY: 2-D C,P)
-    void *out;                 // y, or m for DWONLY
+    CUtensorMap tmap_out;      // y: 4-D K,Wo,Ho,N box (64,tile_w,tile_h,1) or 2-D K,P box (64,128)
+    void *out;                 // m for DWONLY (direct stores)
     const uint8_t *wp_img;     // B operand image (K rows, swizzled, K-major)
-    const float *wdw;          // DW taps [C/8][k*k][8]
+    const uint4 *wdw;          // DW taps, storage dtype, [k*k][C/8] x 8 channels
     const float *s1, *b1, *s2, *b2;
     unsigned *err;
     unsigned long long wait_limit_ns;
@@ -63,8 +64,8 @@ struct Args {
     int in_rows, in_cols;
     int chunk_c, nchunks, stages, n_dw_warps;
     int act1, act2;
-    uint32_t tmem_cols, idesc, wp_img_bytes, in_stage_bytes, a_bytes;
-    uint32_t off_b, off_a, off_in, in_stage_stride, off_wdw, off_sb, off_bar;
+    uint32_t tmem_cols, idesc, wp_img_bytes, in_stage_bytes;
+    uint32_t off_b, off_a, off_in, in_stage_stride, off_out, off_wdw, off_sb, off_bar;
 };
 
 struct Bars {
@@ -81,27 +82,28 @@ struct Bars {
     }
 };
 constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 2 * kMaxChunks + 4 + 2) + 16;
+constexpr int kOutBlock = kTileM * 128;   // bytes of one 64-channel block of the output stage
 
-template <typename T>
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8]) {
-    const T *e = reinterpret_cast<const T *>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; i++) v[i] = Storage<T>::to_f(e[i]);
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
-template <typename T>
-__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
-    uint4 u;
-    T *e = reinterpret_cast<T *>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; i++) e[i] = Storage<T>::from_f(v[i]);
-    return u;
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
-// One DW work unit: kR consecutive output pixels of one tile row, 8 channels.
+// One DW work unit: kR consecutive output pixels of one tile row, 8 channels.  Products of
+// 16-bit inputs and 16-bit taps are exact; sums are fp32 (fma.rn.f32.{f16,bf16}).
 template <typename T, int KS, int S, int MODE>
 __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_t stage_saddr,
-                                        const float *wdw_s, const float *s1_s, const float *b1_s,
+                                        uint32_t wdw_saddr, const float *s1_s, const float *b1_s,
                                         uint32_t a_saddr, int n, int ho0, int wo0) {
     const int nv = a.chunk_c >> 3;
     const int v = u % nv;
@@ -112,6 +114,7 @@ __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_
     const int c_glob = chunk * a.chunk_c + v * 8;
     const uint32_t row_bytes = (uint32_t)a.in_cols * a.chunk_c * 2;
     const uint32_t px_bytes = (uint32_t)a.chunk_c * 2;
+    const uint32_t tap_stride = (uint32_t)a.C * 2;   // bytes between taps of the weight image
 
     float acc[kR][8];
 #pragma unroll
@@ -119,62 +122,53 @@ __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_
 #pragma unroll
         for (int c = 0; c < 8; c++) acc[jj][c] = 0.0f;
 
-    const float4 *wv = reinterpret_cast<const float4 *>(wdw_s) + (size_t)(c_glob >> 3) * KS * KS * 2;
+    const uint32_t wbase = wdw_saddr + (uint32_t)c_glob * 2;
 #pragma unroll
     for (int i = 0; i < KS; i++) {
-        float w[KS][8];
+        uint4 w[KS];
 #pragma unroll
-        for (int t = 0; t < KS; t++) {
-            float4 lo = wv[(i * KS + t) * 2], hi = wv[(i * KS + t) * 2 + 1];
-            w[t][0] = lo.x; w[t][1] = lo.y; w[t][2] = lo.z; w[t][3] = lo.w;
-            w[t][4] = hi.x; w[t][5] = hi.y; w[t][6] = hi.z; w[t][7] = hi.w;
-        }
+        for (int t = 0; t < KS; t++) w[t] = lds128(wbase + (uint32_t)(i * KS + t) * tap_stride);
         const uint32_t rbase = stage_saddr + (uint32_t)(r * S + i) * row_bytes +
                                (uint32_t)(oc0 * S) * px_bytes + (uint32_t)v * 16;
 #pragma unroll
         for (int q = 0; q < (kR - 1) * S + KS; q++) {
-            uint4 raw;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                         : "r"(rbase + (uint32_t)q * px_bytes));
-            float xv[8];
-            unpack8<T>(raw, xv);
+            const uint4 x = lds128(rbase + (uint32_t)q * px_bytes);
 #pragma unroll
             for (int jj = 0; jj < kR; jj++) {
                 const int t = q - jj * S;
                 if (t >= 0 && t < KS) {
-#pragma unroll
-                    for (int c = 0; c < 8; c++) acc[jj][c] = fmaf(xv[c], w[t][c], acc[jj][c]);
+                    Fma16<T>::fma2(acc[jj][0], acc[jj][1], x.x, w[t].x);
+                    Fma16<T>::fma2(acc[jj][2], acc[jj][3], x.y, w[t].y);
+                    Fma16<T>::fma2(acc[jj][4], acc[jj][5], x.z, w[t].z);
+                    Fma16<T>::fma2(acc[jj][6], acc[jj][7], x.w, w[t].w);
                 }
             }
         }
     }
-    float sc[8], bi[8];
-#pragma unroll
-    for (int c = 0; c < 8; c++) {
-        sc[c] = s1_s[c_glob + c];
-        bi[c] = b1_s[c_glob + c];
-    }
+    const float4 sc0 = *reinterpret_cast<const float4 *>(s1_s + c_glob);
+    const float4 sc1 = *reinterpret_cast<const float4 *>(s1_s + c_glob + 4);
+    const float4 bi0 = *reinterpret_cast<const float4 *>(b1_s + c_glob);
+    const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
+    const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
+    const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
 #pragma unroll
     for (int jj = 0; jj < kR; jj++) {
         const int oc = oc0 + jj;
         if (oc >= a.tile_w) break;
-        float o[8];
+        uint32_t pk[4];
 #pragma unroll
-        for (int c = 0; c < 8; c++) o[c] = act_apply(fmaf(sc[c], acc[jj][c], bi[c]), a.act1);
-        uint4 packed = pack8<T>(o);
+        for (int c = 0; c < 4; c++)
+            pk[c] = Pack2<T>::run(fmaf(sc[2 * c], acc[jj][2 * c], bi[2 * c]),
+                                  fmaf(sc[2 * c + 1], acc[jj][2 * c + 1], bi[2 * c + 1]), a.act1);
         if (MODE == FUSED) {
             const int m_row = r * a.tile_w + oc;
-            const uint32_t off = sw128_offset(m_row, c_glob, kTileM, 2);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a_saddr + off),
-                         "r"(packed.x), "r"(packed.y), "r"(packed.z), "r"(packed.w)
-                         : "memory");
+            sts128(a_saddr + sw128_offset(m_row, c_glob, kTileM, 2), pk[0], pk[1], pk[2], pk[3]);
         } else {
             const int ho = ho0 + r, wo = wo0 + oc;
             if (ho < a.Ho && wo < a.Wo) {
                 T *dst = static_cast<T *>(a.out) +
                          (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
-                *reinterpret_cast<uint4 *>(dst) = packed;
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
     }
@@ -200,7 +194,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
     const bool has_mma = MODE != DWONLY;
     const bool has_dw = MODE != PWONLY;
 
-    float *wdw_s = reinterpret_cast<float *>(base_g + a.off_wdw);
+    uint4 *wdw_s = reinterpret_cast<uint4 *>(base_g + a.off_wdw);
     float *sb_s = reinterpret_cast<float *>(base_g + a.off_sb);
     float *s1_s = sb_s, *b1_s = sb_s + a.C, *s2_s = sb_s + 2 * a.C, *b2_s = sb_s + 2 * a.C + a.K;
     const uint32_t bar_base = base_s + a.off_bar;
@@ -210,7 +204,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
 
     // ---- prologue: weights/scales to shared memory, barriers, TMEM
     if (has_dw) {
-        const int nw = a.C * KS * KS;
+        const int nw = a.C * KS * KS / 8;
         for (int i = threadIdx.x; i < nw; i += blockDim.x) wdw_s[i] = a.wdw[i];
     }
     for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
@@ -368,51 +362,67 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
         __syncwarp();
     } else if (warp >= 2 && warp < 2 + kEpiWarps && has_mma) {
         // ===================================================== epilogue
+        // TMEM -> registers -> scale/bias/act -> 16-bit -> 128B-swizzled staging tile in shared
+        // memory -> one TMA tensor store per 64-channel block (full lines, clipped at the edges)
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        const bool issuer = warp == 2 && lane == 0;
+        const uint32_t out_s = base_s + a.off_out;
+        const int nkb_out = (a.K + 63) / 64;
+        const uint32_t swz = (uint32_t)(row & 7);
+        const uint32_t row_s = out_s + (uint32_t)row * 128;
         int lt = 0;
-        T *y = static_cast<T *>(a.out);
         for (long long t = blockIdx.x; t < a.num_tiles; t += gridDim.x, lt++) {
             const int ab = lt & 1;
-            if (!mbar_wait(bars.accfull + 8 * ab, (uint32_t)(lt >> 1) & 1u, abort_flag, a.err, lim))
-                break;
+            const bool ok =
+                mbar_wait(bars.accfull + 8 * ab, (uint32_t)(lt >> 1) & 1u, abort_flag, a.err, lim);
+            if (issuer) bulk_wait_group_read<0>();   // staging free: the last store has read it
+            if (named_barrier_or(1, 32 * kEpiWarps, !ok)) break;
             tc_fence_after();
-            long long pix = -1;
-            if (MODE == PWONLY) {
-                long long p = t * kTileM + row;
-                if (p < a.P) pix = p;
-            } else {
-                int n, ho0, wo0;
-                tile_coords(a, t, n, ho0, wo0);
-                const int r = row / a.tile_w, oc = row % a.tile_w;
-                if (row < a.tile_h * a.tile_w && ho0 + r < a.Ho && wo0 + oc < a.Wo)
-                    pix = ((long long)n * a.Ho + ho0 + r) * a.Wo + wo0 + oc;
-            }
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
             for (int c0 = 0; c0 < a.K; c0 += 16) {
                 uint32_t rr[16];
                 tmem_ld16(taddr + (uint32_t)c0, rr);
                 tmem_ld_wait();
-                if (pix >= 0) {
-                    float o[16];
+                uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        o[i] = act_apply(fmaf(s2_s[c0 + i], __uint_as_float(rr[i]), b2_s[c0 + i]), a.act2);
-                    float lo[8], hi[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        lo[i] = o[i];
-                        hi[i] = o[8 + i];
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(y + pix * a.K + c0);
-                    dst[0] = pack8<T>(lo);
-                    dst[1] = pack8<T>(hi);
+                for (int i4 = 0; i4 < 4; i4++) {
+                    const float4 sc = *reinterpret_cast<const float4 *>(s2_s + c0 + 4 * i4);
+                    const float4 bi = *reinterpret_cast<const float4 *>(b2_s + c0 + 4 * i4);
+                    pk[2 * i4] = Pack2<T>::run(fmaf(sc.x, __uint_as_float(rr[4 * i4]), bi.x),
+                                               fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y),
+                                               a.act2);
+                    pk[2 * i4 + 1] =
+                        Pack2<T>::run(fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z),
+                                      fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w), a.act2);
                 }
+                const uint32_t blk = (uint32_t)(c0 >> 6) * kOutBlock;
+                const uint32_t ch = (uint32_t)((c0 & 63) >> 3);
+                sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+                sts128(row_s + blk + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.accempty + 8 * ab);
+            if (lane == 0) mbar_arrive(bars.accempty + 8 * ab);   // TMEM buffer may be reused
+            fence_proxy_async_smem();                              // staging visible to the TMA
+            named_barrier(1, 32 * kEpiWarps);
+            if (issuer) {
+                if (MODE == PWONLY) {
+                    for (int kb = 0; kb < nkb_out; kb++)
+                        tma_store_2d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
+                                     (int)(t * kTileM));
+                } else {
+                    int n, ho0, wo0;
+                    tile_coords(a, t, n, ho0, wo0);
+                    for (int kb = 0; kb < nkb_out; kb++)
+                        tma_store_4d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64, wo0,
+                                     ho0, n);
+                }
+                bulk_commit_group();
+            }
         }
+        if (issuer) bulk_wait_group<0>();
     } else if (warp >= kFirstDwWarp && has_dw) {
         // ===================================================== DW warps
         const int tid = (warp - kFirstDwWarp) * 32 + lane;
@@ -438,7 +448,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
                 }
                 const uint32_t stage_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
                 for (int u = tid; u < units; u += nthr)
-                    dw_unit<T, KS, S, MODE>(a, u, j, stage_s, wdw_s, s1_s, b1_s, a_s, n, ho0, wo0);
+                    dw_unit<T, KS, S, MODE>(a, u, j, stage_s, base_s + a.off_wdw, s1_s, b1_s, a_s, n,
+                                            ho0, wo0);
                 if (MODE == FUSED) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -486,8 +497,8 @@ uint32_t pow2_cols(int k2) {
 
 // Shared-memory layout of one mode for a plan.  Returns total bytes (incl. alignment slack).
 struct Layout {
-    uint32_t off_b, off_a, off_in, in_stage_bytes, in_stage_stride, off_wdw, off_sb, off_bar,
-        total;
+    uint32_t off_b, off_a, off_out, off_in, in_stage_bytes, in_stage_stride, off_wdw, off_sb,
+        off_bar, total;
     int stages;
 };
 
@@ -496,15 +507,17 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
     const int C = cm, K = d->k_out, nkb = (C + 63) / 64;
     const uint32_t b_bytes = mode == DWONLY ? 0u : (uint32_t)nkb * K * 128;
     const uint32_t a_bytes = mode == FUSED ? (uint32_t)nkb * kTileM * 128 : 0u;
+    const uint32_t out_bytes = mode == DWONLY ? 0u : (uint32_t)((K + 63) / 64) * kOutBlock;
     L.off_b = 0;
     L.off_a = align_up(b_bytes, 1024);
-    L.off_in = align_up(L.off_a + a_bytes, 1024);
+    L.off_out = align_up(L.off_a + a_bytes, 1024);
+    L.off_in = align_up(L.off_out + out_bytes, 1024);
     if (mode == PWONLY)
         L.in_stage_bytes = (uint32_t)nkb * kTileM * 128;
     else
         L.in_stage_bytes = (uint32_t)p.in_rows * p.in_cols * p.chunk_c * 2;
     L.in_stage_stride = align_up(L.in_stage_bytes, 1024);
-    const uint32_t wdw = mode == PWONLY ? 0u : (uint32_t)C * d->ksize * d->ksize * 4;
+    const uint32_t wdw = mode == PWONLY ? 0u : (uint32_t)C * d->ksize * d->ksize * 2;
     const uint32_t sb = (uint32_t)(2 * C + 2 * K) * 4;
     const uint32_t tail = align_up(wdw, 16) + align_up(sb, 16) + kBarBytes + 16 + 1024;
     int stages = mode == PWONLY ? 4 : p.stages;
@@ -624,26 +637,16 @@ fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_hos
             uint32_t off = sw128_offset(n, c, K, 2);
             memcpy(&img[off], &wp16[(size_t)n * C + c], 2);
         }
-    // DW taps as fp32 [C/8][k*k][8]
-    std::vector<float> wdw((size_t)C * KS * KS);
+    // DW taps in the storage dtype, tap-major: [k*k][C] (lane v of a warp reads channels
+    // 8v..8v+7 of one tap as one 16-byte vector, consecutive lanes consecutive vectors)
+    std::vector<uint16_t> wdw((size_t)C * KS * KS);
+    const uint16_t *w1b = static_cast<const uint16_t *>(w1_host);
     for (int c = 0; c < C; c++)
-        for (int t = 0; t < KS * KS; t++) {
-            float v;
-            uint16_t bits = static_cast<const uint16_t *>(w1_host)[(size_t)c * KS * KS + t];
-            if (d.dtype == FCM_F16) {
-                __half hv;
-                memcpy(&hv, &bits, 2);
-                v = __half2float(hv);
-            } else {
-                uint32_t u = (uint32_t)bits << 16;
-                memcpy(&v, &u, 4);
-            }
-            wdw[((size_t)(c / 8) * KS * KS + t) * 8 + (c % 8)] = v;
-        }
+        for (int t = 0; t < KS * KS; t++) wdw[(size_t)t * C + c] = w1b[(size_t)c * KS * KS + t];
     if (cudaMalloc(&h->wp_img, h->wp_img_bytes) != cudaSuccess ||
         cudaMemcpy(h->wp_img, img.data(), h->wp_img_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMalloc(reinterpret_cast<void **>(&h->w1dw_img), wdw.size() * 4) != cudaSuccess ||
-        cudaMemcpy(h->w1dw_img, wdw.data(), wdw.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        cudaMalloc(&h->w1dw_img, wdw.size() * 2) != cudaSuccess ||
+        cudaMemcpy(h->w1dw_img, wdw.data(), wdw.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess)
         return fcm_fail(FCM_ERR_CUDA, "tensor-core weight images: %s",
                         cudaGetErrorString(cudaGetLastError()));
     return FCM_OK;
@@ -707,9 +710,29 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
         a.num_tiles = p.num_tiles;
     }
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (mode == PWONLY) {
+        cuuint64_t gdim[2] = {(cuuint64_t)d.k_out, (cuuint64_t)a.P};
+        cuuint64_t gstride[1] = {(cuuint64_t)d.k_out * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)kTileM};
+        cuuint32_t estr[2] = {1, 1};
+        cr = enc(&a.tmap_out, dt, 2, out, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (mode == FUSED) {
+        cuuint64_t gdim[4] = {(cuuint64_t)d.k_out, (cuuint64_t)h->wo, (cuuint64_t)h->ho,
+                              (cuuint64_t)d.n};
+        cuuint64_t gstride[3] = {(cuuint64_t)d.k_out * 2, (cuuint64_t)h->wo * d.k_out * 2,
+                                 (cuuint64_t)h->ho * h->wo * d.k_out * 2};
+        cuuint32_t box[4] = {64, (cuuint32_t)p.tile_w, (cuuint32_t)p.tile_h, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        cr = enc(&a.tmap_out, dt, 4, out, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     a.out = out;
     a.wp_img = static_cast<const uint8_t *>(h->wp_img);
-    a.wdw = h->w1dw_img;
+    a.wdw = static_cast<const uint4 *>(h->w1dw_img);
     a.s1 = h->s1;
     a.b1 = h->b1;
     a.s2 = h->s2;
@@ -738,6 +761,7 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.in_stage_stride = L.in_stage_stride;
     a.off_b = L.off_b;
     a.off_a = L.off_a;
+    a.off_out = L.off_out;
     a.off_in = L.off_in;
     a.off_wdw = L.off_wdw;
     a.off_sb = L.off_sb;
