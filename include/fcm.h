@@ -128,6 +128,23 @@ FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, v
 FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
                         void *stream);
 
+/* Layer-by-layer evaluation that allocates nothing: the same result as fcm_run with
+ * FCM_MODE_UNFUSED, but the intermediate is kept in a fixed 16 MiB device array compiled into
+ * the library instead of a buffer the handle allocates on first use.  The paper has no
+ * counterpart; it exists for callers that cannot call cudaMalloc while they run -- a serving
+ * loop whose memory is budgeted up front, a host thread that must not take the allocator's
+ * locks or trigger its implicit synchronisation, a process whose device memory belongs to
+ * another allocator.  `in`/`out` as for FCM_MODE_UNFUSED (caller-owned device memory).
+ *  - Rejects (FCM_ERR_UNSUPPORTED) an intermediate N*Ho*Wo*Cm*element-size above 16 MiB.
+ *  - The array exists once per device that loads the library and is kept until exit.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *    make that first call before any stream capture.  The current device must be the
+ *    handle's device.
+ *  - Every call uses the same array and leaves its intermediate there; each call rewrites all
+ *    of it before reading it.  Calls that overlap on the GPU (other streams, other handles,
+ *    other threads) race on it: serialise them. */
+FCM_API fcm_status fcm_run_unfused_static(fcm_handle *h, const void *in, void *out, void *stream);
+
 /* Synchronize `stream`, then read and clear the handle's device error word.  Returns
  * FCM_ERR_TIMEOUT if a bounded wait in a kernel ran out, FCM_ERR_DEVICE_FAULT if a kernel's
  * own check failed, FCM_OK otherwise. */

@@ -19,6 +19,7 @@ __all__ = [
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "EXPORTED_SYMBOLS",
+    "fcm_run_unfused_static",
     "DTYPES", "ACTS", "MODES",
 ]
 
@@ -38,7 +39,7 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2}
 EXPORTED_SYMBOLS = (
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
-    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma",
+    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_run_unfused_static",
 )
 
 
@@ -87,11 +88,12 @@ def load_library(path: str | None = None):
                                    ctypes.POINTER(vp)]
         lib.fcm_run.argtypes = [vp, i, vp, vp, vp]
         lib.fcm_run_host.argtypes = [vp, i, vp, vp, vp]
+        lib.fcm_run_unfused_static.argtypes = [vp, vp, vp, vp]
         lib.fcm_check.argtypes = [vp, vp]
         lib.fcm_plan.argtypes = [vp, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_plan_desc.argtypes = [ctypes.POINTER(FcmDesc), i, i, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_tensor_bytes.argtypes = [ctypes.POINTER(FcmDesc)] + [ctypes.POINTER(ctypes.c_size_t)] * 3
-        for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan",
+        for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_run_unfused_static", "fcm_check", "fcm_plan",
                   "fcm_plan_desc", "fcm_tensor_bytes"):
             getattr(lib, f).restype = i
         lib.fcm_destroy.argtypes = [vp]
@@ -147,6 +149,12 @@ def fcm_run(handle: int, mode: int, inp: int, out: int, stream: int = 0) -> None
 
 def fcm_run_host(handle: int, mode: int, host_in: int, host_out: int, stream: int = 0) -> None:
     _check(load_library().fcm_run_host(handle, mode, host_in, host_out, stream))
+
+
+def fcm_run_unfused_static(handle: int, inp: int, out: int, stream: int = 0) -> None:
+    """Layer-by-layer evaluation with the intermediate in the library's fixed device array:
+    allocates nothing (for callers that cannot call cudaMalloc); see include/fcm.h."""
+    _check(load_library().fcm_run_unfused_static(handle, inp, out, stream))
 
 
 def fcm_check(handle: int, stream: int = 0) -> None:
