@@ -68,6 +68,12 @@ int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why
 fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
                        TcPlan *tc);
 
+// tc_b2b.cu: dense k x k -> 1x1 on tcgen05
+int fcm_b2b_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);
+fcm_status fcm_b2b_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
+                        TcPlan *tc);
+fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_host);
+
 // simt_kernels.cu
 cudaError_t launch_conv1_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st);
 cudaError_t launch_pw_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st);

@@ -225,18 +225,20 @@ _TID = {"x": 1, "w1": 2, "wp": 3, "s1": 4, "b1": 5, "s2": 6, "b2": 7}
 
 def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) -> Case:
     """Draw a case.  kind: None -> the workload's own distribution ("uniform" or "normal");
-    "integer" -> small integers chosen so that every partial sum is exact in fp32 and the
-    intermediate is exact in the storage format (bit-exact checks)."""
+    "integer" -> small integers (x in [-3,3], weights in [-2,2]) chosen so that every partial
+    sum is exact in fp32 and the intermediate is exact in the storage format (bit-exact
+    checks); "integer1" -> the same with x and weights in [-1,1], for wide dense layers."""
     seed = BASE_SEED if seed is None else seed
     kind = wl.dist if kind is None else kind
     sh = wl.shapes()
     cnt = {name: int(np.prod(sh[name])) for name in _TID}
     fan1, fan2 = wl.fan_in()
     d = wl.dtype
-    if kind == "integer":
-        x = integers(seed, _TID["x"], cnt["x"], -3, 3)
-        w1 = integers(seed, _TID["w1"], cnt["w1"], -2, 2)
-        wp = integers(seed, _TID["wp"], cnt["wp"], -2, 2)
+    if kind in ("integer", "integer1"):
+        xr, wr = (3, 2) if kind == "integer" else (1, 1)
+        x = integers(seed, _TID["x"], cnt["x"], -xr, xr)
+        w1 = integers(seed, _TID["w1"], cnt["w1"], -wr, wr)
+        wp = integers(seed, _TID["wp"], cnt["wp"], -wr, wr)
         s1 = np.ones(cnt["s1"])
         s2 = np.ones(cnt["s2"])
         b1 = integers(seed, _TID["b1"], cnt["b1"], -2, 2)
@@ -262,12 +264,13 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
                 f32(s2, "s2"), f32(b2, "b2"))
 
 
-def integer_safe(wl: Workload) -> bool:
-    """True when the "integer" case of `wl` is exact end to end: fp32 partial sums stay below
-    2^24 and the intermediate (|m| <= k*k*3*2 + 2, before the activation) is exactly
+def integer_safe(wl: Workload, kind: str = "integer") -> bool:
+    """True when the integer case of `wl` is exact end to end: fp32 partial sums stay below
+    2^24 and the intermediate (|m| <= k*k*max|x*w| + 2, before the activation) is exactly
     representable in the storage format (2^8 for bf16, 2^11 for f16)."""
     k = wl.ksize
-    per1 = k * k * (wl.c if wl.conv1 == "dense" else 1) * 6 + 2
+    prod = 6 if kind == "integer" else 1
+    per1 = k * k * (wl.c if wl.conv1 == "dense" else 1) * prod + 2
     lim = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8}[wl.dtype]
     mid_max = min(per1, 6) if wl.act1 == "relu6" else per1
-    return per1 < (1 << 24) and mid_max <= lim and wl.cm * mid_max * 2 + 2 < (1 << 24)
+    return per1 < (1 << 24) and mid_max <= lim and wl.cm * mid_max * (prod // 3 + 1) + 2 < (1 << 24)

@@ -35,20 +35,21 @@ def module_or_skip(case, kernel):
         raise
 
 
-def integer_variant(wl: wk.Workload) -> wk.Workload:
-    """Shrink the channel count where needed so that the integer case is exact end to end."""
+def integer_variant(wl: wk.Workload) -> tuple[wk.Workload, str]:
+    """The integer kind that keeps the case exact end to end (+-1 values for wide dense
+    layers)."""
     if wk.integer_safe(wl):
-        return wl
-    if wl.conv1 == "dense":
-        return wl.with_(c=16, mid=16 if wl.mid else 0)
+        return wl, "integer"
+    if wk.integer_safe(wl, "integer1"):
+        return wl, "integer1"
     raise AssertionError(wl)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
 def test_integer_bitexact_fused_and_unfused(cuda, wl, kernel):
-    small = integer_variant(reduced(wl, n=2, hw=min(wl.h, 30)))
-    case = wk.make_case(small, kind="integer")
+    small, kind = integer_variant(reduced(wl, n=2, hw=min(wl.h, 30)))
+    case = wk.make_case(small, kind=kind)
     mod = module_or_skip(case, kernel)
     ref = oracle_fused(case)
     for mode in ("fused", "unfused"):
@@ -120,14 +121,30 @@ def test_edge_shapes(cuda, shape, kernel):
         assert_bitexact(got, oracle_fused(icase), dt)
 
 
+DENSE_EDGE = [  # (N, H, W, C, mid, K, k, p, dtype, act1, act2)
+    (2, 9, 13, 32, 32, 48, 3, 1, "f16", "relu", "relu6"),
+    (2, 9, 13, 64, 32, 48, 3, 1, "f16", "relu", "relu6"),
+    (1, 11, 60, 128, 64, 64, 5, 2, "bf16", "relu", "none"),
+    (3, 7, 100, 64, 16, 32, 3, 1, "f16", "none", "relu"),
+    (1, 5, 21, 64, 48, 16, 1, 0, "bf16", "relu6", "relu"),
+]
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_dense_edge_shapes(cuda, kernel):
-    wl = wk.Workload("dense_edge", 2, 9, 13, 32, 48, "dense", 3, 1, 1, "relu", "relu6", "f16",
-                     "normal", mid=32)
+@pytest.mark.parametrize("shape", DENSE_EDGE, ids=lambda s: "x".join(map(str, s[:8])) + s[8])
+def test_dense_edge_shapes(cuda, shape, kernel):
+    N, H, W, C, mid, K, k, p, dt, a1, a2 = shape
+    wl = wk.Workload("dense_edge", N, H, W, C, K, "dense", k, 1, p, a1, a2, dt, "normal", mid=mid)
     case = wk.make_case(wl, seed=5)
     mod = module_or_skip(case, kernel)
     got, _ = run_case(case, "fused", module=mod)
-    assert_parity(got, oracle_fused(case), "f16", 32)
+    assert_parity(got, oracle_fused(case), dt, mid)
+    got_u, _ = run_case(case, "unfused", module=mod)
+    assert_parity(got_u, oracle_fused(case), dt, mid)
+    if wk.integer_safe(wl, "integer1"):
+        icase = wk.make_case(wl, seed=6, kind="integer1")
+        got, _ = run_case(icase, "fused", module=make_module(icase, kernel))
+        assert_bitexact(got, oracle_fused(icase), dt)
 
 
 def test_run_host_matches_run(cuda):

@@ -66,6 +66,9 @@ def test_integer_case_exactness():
     assert np.all(f["x"] == np.round(f["x"])) and np.abs(f["x"]).max() <= 3
     assert wk.integer_safe(wl)
     assert not wk.integer_safe(wk.BY_NAME["b2b_dense3x3_f16"])   # 9*64*6 > 2^11
+    assert wk.integer_safe(wk.BY_NAME["b2b_dense3x3_f16"], "integer1")   # 9*64*1 + 2 < 2^11
+    c1 = wk.make_case(wk.BY_NAME["b2b_dense3x3_f16"].with_(n=1, h=4, w=4), kind="integer1")
+    assert set(np.unique(c1.f64()["x"])) <= {-1.0, 0.0, 1.0}
 
 
 def test_min_bytes_closed_form():
