@@ -27,6 +27,7 @@ struct TcPlan {
     int threads = 0;
     int ctas = 0;
     int tmem_cols = 0;
+    int out_bufs = 1;             // DW->PW output staging tiles (2: stores overlap the next tile)
 };
 
 struct fcm_handle {

@@ -96,37 +96,49 @@ __device__ __forceinline__ uint64_t shifted_desc(uint32_t saddr) { return sw128_
 
 // TMEM accumulator (128 lanes x ncols fp32) -> scale/bias/act -> 16-bit -> a 128-row,
 // 128B-swizzled K-major image in shared memory (64-channel blocks of kBlk bytes).
+template <typename T, int ACT>
+__device__ __forceinline__ void emit16(const uint32_t (&rr)[16], int cc, const float *sc_s,
+                                       const float *bi_s, uint32_t dst_s, int row) {
+    const uint32_t swz = (uint32_t)(row & 7);
+    uint32_t pk[8];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; i4++) {
+        const float4 s = *reinterpret_cast<const float4 *>(sc_s + cc + 4 * i4);
+        const float4 b = *reinterpret_cast<const float4 *>(bi_s + cc + 4 * i4);
+        pk[2 * i4] = Pack2<T>::template run<ACT>(fmaf(s.x, __uint_as_float(rr[4 * i4]), b.x),
+                                                 fmaf(s.y, __uint_as_float(rr[4 * i4 + 1]), b.y));
+        pk[2 * i4 + 1] = Pack2<T>::template run<ACT>(fmaf(s.z, __uint_as_float(rr[4 * i4 + 2]), b.z),
+                                                     fmaf(s.w, __uint_as_float(rr[4 * i4 + 3]), b.w));
+    }
+    const uint32_t base = dst_s + (uint32_t)(cc >> 6) * kBlk + (uint32_t)row * 128;
+    const uint32_t ch = (uint32_t)((cc & 63) >> 3);
+    sts128(base + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+    sts128(base + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
+}
+
+// TMEM accumulator (128 lanes x ncols fp32, ncols a multiple of 16) -> scale/bias/act ->
+// 16-bit -> a 128-row, 128B-swizzled K-major image in shared memory (64-channel blocks of kBlk
+// bytes).  Two loads of 16 columns, then one wait.
+template <typename T, int ACT>
+__device__ __forceinline__ void acc_to_smem_act(uint32_t taddr_row, int ncols, const float *sc_s,
+                                                const float *bi_s, uint32_t dst_s, int row) {
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
+        uint32_t ra[16], rb[16];
+        const bool two = c0 + 16 < ncols;
+        tmem_ld16(taddr_row + (uint32_t)c0, ra);
+        if (two) tmem_ld16(taddr_row + (uint32_t)(c0 + 16), rb);
+        tmem_ld_wait();
+        emit16<T, ACT>(ra, c0, sc_s, bi_s, dst_s, row);
+        if (two) emit16<T, ACT>(rb, c0 + 16, sc_s, bi_s, dst_s, row);
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void acc_to_smem(uint32_t taddr_row, int ncols, const float *sc_s,
                                             const float *bi_s, int act, uint32_t dst_s, int row) {
-    const uint32_t swz = (uint32_t)(row & 7);
-    for (int c0 = 0; c0 < ncols; c0 += 32) {
-        const bool two = c0 + 16 < ncols;
-        uint32_t rr[32];
-        tmem_ld16(taddr_row + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(&rr[0]));
-        if (two) tmem_ld16(taddr_row + (uint32_t)c0 + 16u, *reinterpret_cast<uint32_t(*)[16]>(&rr[16]));
-        tmem_ld_wait();
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-            if (h == 1 && !two) break;
-            const int cc = c0 + 16 * h;
-            uint32_t pk[8];
-#pragma unroll
-            for (int i4 = 0; i4 < 4; i4++) {
-                const float4 s = *reinterpret_cast<const float4 *>(sc_s + cc + 4 * i4);
-                const float4 b = *reinterpret_cast<const float4 *>(bi_s + cc + 4 * i4);
-                const uint32_t *r4 = &rr[16 * h + 4 * i4];
-                pk[2 * i4] = Pack2<T>::run(fmaf(s.x, __uint_as_float(r4[0]), b.x),
-                                           fmaf(s.y, __uint_as_float(r4[1]), b.y), act);
-                pk[2 * i4 + 1] = Pack2<T>::run(fmaf(s.z, __uint_as_float(r4[2]), b.z),
-                                               fmaf(s.w, __uint_as_float(r4[3]), b.w), act);
-            }
-            const uint32_t base = dst_s + (uint32_t)(cc >> 6) * kBlk + (uint32_t)row * 128;
-            const uint32_t ch = (uint32_t)((cc & 63) >> 3);
-            sts128(base + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
-            sts128(base + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
-        }
-    }
+    with_act(act, [&](auto act_tag) {
+        acc_to_smem_act<T, decltype(act_tag)::value>(taddr_row, ncols, sc_s, bi_s, dst_s, row);
+    });
 }
 
 // Called by one thread after its warp group staged a tile: one TMA store per output row of
@@ -144,7 +156,7 @@ __device__ __forceinline__ void store_tile(const Args &a, const CUtensorMap *map
     bulk_commit_group();
 }
 
-template <typename T, int MODE>
+template <typename T, int KS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -199,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
 
     if (warp == 0) {
         // ===================================================== TMA producer
-        int issued_per_stage[kMaxStages];
-        for (int s = 0; s < kMaxStages; s++) issued_per_stage[s] = 0;
+        int issued = 0;   // loads issued so far; load i goes to stage i % stages
         bool ok = true;
         if (lane == 0) {
             mbar_arrive_expect_tx(bars.wbar, a.w1_bytes + (MODE == FUSED ? a.w2_bytes : 0u));
@@ -225,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
                     tma_load_4d(dst + (uint32_t)kb * a.plane_bytes, &a.tmap_in, bars.full + 8 * s,
                                 kb * 64, -a.pad, ho0 - a.pad, n);
             }
-            issued_per_stage[s]++;
+            issued++;
             __syncwarp();
             if (++s == a.stages) {
                 s = 0;
@@ -234,10 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
         }
         if (!ok) {
             volatile int no_abort = 0;
-            for (int q = 0; q < a.stages; q++)
-                if (issued_per_stage[q] > 0)
-                    mbar_wait(bars.full + 8 * q, (uint32_t)(issued_per_stage[q] - 1) & 1u, &no_abort,
-                              a.err, lim);
+            for (int q = 0; q < a.stages && q < issued; q++) {
+                const int nq = (issued - 1 - q) / a.stages + 1;   // loads that went to stage q
+                mbar_wait(bars.full + 8 * q, (uint32_t)(nq - 1) & 1u, &no_abort, a.err, lim);
+            }
             mbar_wait(bars.wbar, 0, &no_abort, a.err, lim);
         }
     } else if (warp == 1) {
@@ -258,22 +269,28 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
                 }
                 tc_fence_after();
                 if (lane == 0) {
+                    // descriptors are advanced from two bases; the tap loops unroll (KS is a
+                    // template parameter), so each MMA costs a couple of integer adds to issue
                     const uint32_t in_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
                     const uint32_t d = tmem_base + acc1_col + (uint32_t)b * (uint32_t)a.Cm;
-                    uint32_t acc = 0;
-                    for (int r = 0; r < a.ks; r++)
-                        for (int tt = 0; tt < a.ks; tt++)
-                            for (int kb = 0; kb < a.nkb_in; kb++)
-                                for (int k16 = 0; k16 < 4; k16++) {
-                                    const uint32_t as = in_s + (uint32_t)kb * a.plane_bytes +
-                                                        (uint32_t)(r * a.P + tt) * 128u + (uint32_t)k16 * 32u;
-                                    const uint32_t bs = w1_s +
-                                                        (uint32_t)(((r * a.ks + tt) * a.nkb_in + kb) * a.Cm) * 128u +
-                                                        (uint32_t)k16 * 32u;
-                                    mma_f16(d, shifted_desc(as), sw128_kmajor_desc(bs),
-                                            a.idesc1, acc);
-                                    acc = 1;
-                                }
+                    const uint64_t a_base = shifted_desc(in_s);
+                    const uint64_t b_base = sw128_kmajor_desc(w1_s);
+                    const uint32_t w_kb = (uint32_t)a.Cm * 128u;            // one 64-channel block of a tap
+                    const uint32_t w_tap = (uint32_t)a.nkb_in * w_kb;       // one tap
+#pragma unroll
+                    for (int r = 0; r < KS; r++)
+#pragma unroll
+                        for (int tt = 0; tt < KS; tt++)
+                            for (int kb = 0; kb < a.nkb_in; kb++) {
+                                const uint64_t ad = desc_advance(
+                                    a_base, (uint32_t)kb * a.plane_bytes + (uint32_t)(r * a.P + tt) * 128u);
+                                const uint64_t bd = desc_advance(
+                                    b_base, (uint32_t)(r * KS + tt) * w_tap + (uint32_t)kb * w_kb);
+#pragma unroll
+                                for (int k16 = 0; k16 < 4; k16++)
+                                    mma_f16(d, desc_advance(ad, 32u * k16), desc_advance(bd, 32u * k16),
+                                            a.idesc1, (r | tt | kb | k16) != 0 ? 1u : 0u);
+                            }
                     mma_commit(bars.empty + 8 * s);
                     mma_commit(bars.acc1full + 8 * b);
                 }
@@ -295,11 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
                 if (lane == 0) {
                     const uint32_t a2_s = base_s + a.off_a2 + (uint32_t)b * (uint32_t)a.nkb_mid * kBlk;
                     const uint32_t d = tmem_base + acc2_col + (uint32_t)b * (uint32_t)a.K;
-                    for (int k16 = 0; k16 < a.Cm / 16; k16++) {
-                        const uint32_t koff = (uint32_t)(k16 & 3) * 32u;
-                        const uint64_t ad = sw128_kmajor_desc(a2_s + (uint32_t)(k16 >> 2) * kBlk + koff);
-                        const uint64_t bd = sw128_kmajor_desc(w2_s + (uint32_t)(k16 >> 2) * (uint32_t)a.K * 128u + koff);
-                        mma_f16(d, ad, bd, a.idesc2, k16 > 0 ? 1u : 0u);
+                    const uint64_t a_base = sw128_kmajor_desc(a2_s), b_base = sw128_kmajor_desc(w2_s);
+                    for (int kb = 0; kb < a.nkb_mid; kb++) {
+                        const uint64_t ad = desc_advance(a_base, (uint32_t)kb * kBlk);
+                        const uint64_t bd = desc_advance(b_base, (uint32_t)kb * (uint32_t)a.K * 128u);
+                        const int n16 = min(4, (a.Cm - 64 * kb) / 16);
+                        for (int k16 = 0; k16 < n16; k16++)
+                            mma_f16(d, desc_advance(ad, 32u * k16), desc_advance(bd, 32u * k16), a.idesc2,
+                                    (kb | k16) != 0 ? 1u : 0u);
                     }
                     mma_commit(bars.a2empty + 8 * b);
                     mma_commit(bars.acc2full + 8 * b);
@@ -529,15 +549,34 @@ fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_ho
 
 namespace {
 
-template <typename T, int MODE>
+template <typename T, int KS, int MODE>
 cudaError_t launch_t(const Args &a, int ctas, uint32_t smem, cudaStream_t st) {
-    auto k = b2b_kernel<T, MODE>;
+    auto k = b2b_kernel<T, KS, MODE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<ctas, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
+template <typename T, int KS>
+cudaError_t dispatch_mode(const Args &a, int mode, int ctas, uint32_t smem, cudaStream_t st) {
+    return mode == FUSED ? launch_t<T, KS, FUSED>(a, ctas, smem, st)
+                         : launch_t<T, KS, CONV1>(a, ctas, smem, st);
+}
+
+template <typename T>
+cudaError_t dispatch_ks(const Args &a, int ks, int mode, int ctas, uint32_t smem, cudaStream_t st) {
+    if (ks == 1) return dispatch_mode<T, 1>(a, mode, ctas, smem, st);
+    if (ks == 3) return dispatch_mode<T, 3>(a, mode, ctas, smem, st);
+    if (ks == 5) return dispatch_mode<T, 5>(a, mode, ctas, smem, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t dispatch_dtype(const Args &a, bool f16, int ks, int mode, int ctas, uint32_t smem,
+                           cudaStream_t st) {
+    return f16 ? dispatch_ks<__half>(a, ks, mode, ctas, smem, st)
+               : dispatch_ks<__nv_bfloat16>(a, ks, mode, ctas, smem, st);
+}
 
 }  // namespace
 
@@ -618,9 +657,5 @@ cudaError_t launch_tc_b2b(const fcm_handle *h, int mode_in, const void *in, void
     a.off_sb = L.off_sb;
     a.off_bar = L.off_bar;
     const int ctas = std::min(a.num_tiles, h->num_sms);
-    if (d.dtype == FCM_F16)
-        return mode == FUSED ? launch_t<__half, FUSED>(a, ctas, L.total, st)
-                             : launch_t<__half, CONV1>(a, ctas, L.total, st);
-    return mode == FUSED ? launch_t<__nv_bfloat16, FUSED>(a, ctas, L.total, st)
-                         : launch_t<__nv_bfloat16, CONV1>(a, ctas, L.total, st);
+    return dispatch_dtype(a, d.dtype == FCM_F16, d.ksize, mode, ctas, L.total, st);
 }

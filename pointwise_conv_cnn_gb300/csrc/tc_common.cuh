@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "fcm_device.cuh"
 
 namespace fcm {
@@ -187,26 +189,56 @@ template <> struct Fma16<__nv_bfloat16> {
     }
 };
 
-// Round two fp32 values to a packed 16-bit pair (round to nearest even), then apply the
-// activation on the pair.  Clamping after rounding equals rounding after clamping because
-// rounding is monotonic and 0 and 6 are exact.
+// Round two fp32 values to a packed 16-bit pair (round to nearest even; `lo` in the low half)
+// and apply activation ACT (0 none, 1 ReLU, 2 ReLU6): the conversion itself clamps at 0
+// (cvt .relu), then ReLU6 takes the minimum with 6 on the pair.  Clamping after rounding
+// equals rounding after clamping because rounding is monotonic and 0 and 6 are exact.  ACT is a
+// template parameter so that the per-element code has no branches.
 template <typename T> struct Pack2;
 template <> struct Pack2<__half> {
-    static __device__ __forceinline__ uint32_t run(float a, float b, int act) {
-        __half2 h = __floats2half2_rn(a, b);
-        if (act != 0) h = __hmax2(h, __float2half2_rn(0.0f));
-        if (act == 2) h = __hmin2(h, __float2half2_rn(6.0f));
-        return *reinterpret_cast<uint32_t *>(&h);
+    template <int ACT>
+    static __device__ __forceinline__ uint32_t run(float lo, float hi) {
+        uint32_t r;
+        if (ACT == 0)
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        else
+            asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        if (ACT == 2) {
+            __half2 h = *reinterpret_cast<__half2 *>(&r);
+            h = __hmin2(h, __float2half2_rn(6.0f));
+            r = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return r;
     }
 };
 template <> struct Pack2<__nv_bfloat16> {
-    static __device__ __forceinline__ uint32_t run(float a, float b, int act) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        if (act != 0) h = __hmax2(h, __float2bfloat162_rn(0.0f));
-        if (act == 2) h = __hmin2(h, __float2bfloat162_rn(6.0f));
-        return *reinterpret_cast<uint32_t *>(&h);
+    template <int ACT>
+    static __device__ __forceinline__ uint32_t run(float lo, float hi) {
+        uint32_t r;
+        if (ACT == 0)
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        else
+            asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        if (ACT == 2) {
+            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&r);
+            h = __hmin2(h, __float2bfloat162_rn(6.0f));
+            r = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return r;
     }
 };
+
+// Calls f(std::integral_constant<int, act>{}) for a runtime activation code 0, 1 or 2, so that a
+// role's loop is compiled once per activation.
+template <typename F>
+__device__ __forceinline__ void with_act(int act, F &&f) {
+    if (act == 0)
+        f(std::integral_constant<int, 0>{});
+    else if (act == 1)
+        f(std::integral_constant<int, 1>{});
+    else
+        f(std::integral_constant<int, 2>{});
+}
 
 // -------------------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
@@ -275,6 +307,13 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     d |= (uint64_t)1 << 46;                        // descriptor version for tcgen05
     d |= (uint64_t)2 << 61;                        // 128-byte swizzle
     return d;
+}
+
+// The descriptor of the operand `bytes` further on (a multiple of 16): the start-address field
+// holds address / 16 in 14 bits and shared memory ends below 2^18 bytes, so the field never
+// carries into the next one.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+    return d + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands K-major.

@@ -26,6 +26,7 @@
 // copies and MMAs before TMEM is released.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <string.h>
 
 #include <algorithm>
@@ -39,7 +40,7 @@ namespace tc {
 
 constexpr int kEpiWarps = 4;
 constexpr int kFirstDwWarp = 2 + kEpiWarps;
-constexpr int kMaxDwWarps = 12;
+constexpr int kMaxDwWarps = 10;   // 16 warps in all: up to 128 registers a thread
 constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);
 constexpr int kR = 4;          // output pixels per DW work unit (along W)
 constexpr int kTileM = 128;    // MMA M: pixels per output tile (padded)
@@ -57,7 +58,7 @@ struct Args {
     const float *s1, *b1, *s2, *b2;
     unsigned *err;
     unsigned long long wait_limit_ns;
-    long long num_tiles;
+    int num_tiles;
     long long P;               // PWONLY: pixel count
     int N, H, W, C, K, Ho, Wo, pad;
     int tile_h, tile_w, tiles_w, tiles_per_img, ngroups;
@@ -66,6 +67,8 @@ struct Args {
     int act1, act2;
     uint32_t tmem_cols, idesc, wp_img_bytes, in_stage_bytes;
     uint32_t off_b, off_a, off_in, in_stage_stride, off_out, off_wdw, off_sb, off_bar;
+    int out_bufs;              // output staging tiles (2: a tile's stores overlap the next tile)
+    uint32_t out_buf_bytes;
 };
 
 struct Bars {
@@ -99,22 +102,48 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
-// One DW work unit: kR consecutive output pixels of one tile row, 8 channels.  Products of
-// 16-bit inputs and 16-bit taps are exact; sums are fp32 (fma.rn.f32.{f16,bf16}).
-template <typename T, int KS, int S, int MODE>
-__device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_t stage_saddr,
-                                        uint32_t wdw_saddr, const float *s1_s, const float *b1_s,
-                                        uint32_t a_saddr, int n, int ho0, int wo0) {
+// Where one DW work unit (kR consecutive output pixels of one tile row, 8 channels) sits in a
+// stage and in the A tile.  None of it depends on the tile or on the channel chunk, so each
+// thread works it out once for the units it owns.
+struct DwUnit {
+    uint32_t x_off;   // byte offset of the unit's first input vector within a stage
+    int m_row0;       // A-tile row of the unit's first output pixel (= pixel index in the tile)
+    int cv;           // first of the unit's 8 channels within a chunk
+    int nvalid;       // output pixels of the unit inside the tile (1..kR)
+    int r, oc0;       // tile row and first tile column of the unit
+};
+
+template <int S>
+__device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
     const int nv = a.chunk_c >> 3;
     const int v = u % nv;
     const int rest = u / nv;
     const int g = rest % a.ngroups;
-    const int r = rest / a.ngroups;
-    const int oc0 = g * kR;
-    const int c_glob = chunk * a.chunk_c + v * 8;
-    const uint32_t row_bytes = (uint32_t)a.in_cols * a.chunk_c * 2;
-    const uint32_t px_bytes = (uint32_t)a.chunk_c * 2;
-    const uint32_t tap_stride = (uint32_t)a.C * 2;   // bytes between taps of the weight image
+    DwUnit d;
+    d.r = rest / a.ngroups;
+    d.oc0 = g * kR;
+    d.cv = v * 8;
+    d.x_off = (uint32_t)((d.r * S) * a.in_cols + d.oc0 * S) * (uint32_t)a.chunk_c * 2u + (uint32_t)v * 16u;
+    d.m_row0 = d.r * a.tile_w + d.oc0;
+    d.nvalid = min(kR, a.tile_w - d.oc0);
+    return d;
+}
+
+// One DW work unit.  Products of 16-bit inputs and 16-bit taps are exact; sums are fp32
+// (fma.rn.f32.{f16,bf16}).  `stage` and `wdw` are shared-memory pointers; the loads are plain
+// C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
+// which clobber memory).
+template <typename T, int KS, int S, int MODE, int ACT>
+__device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chunk,
+                                        const uint8_t *stage, const uint8_t *wdw,
+                                        const float *s1_s, const float *b1_s, uint32_t a_saddr,
+                                        int n, int ho0, int wo0) {
+    const int c_glob = chunk * a.chunk_c + g.cv;
+    const uint32_t px_bytes = (uint32_t)a.chunk_c * 2u;
+    const uint32_t row_bytes = (uint32_t)a.in_cols * px_bytes;
+    const uint32_t tap_bytes = (uint32_t)a.C * 2u;   // bytes between taps of the weight image
+    const uint8_t *xb = stage + g.x_off;
+    const uint8_t *wb = wdw + (uint32_t)c_glob * 2u;
 
     float acc[kR][8];
 #pragma unroll
@@ -122,17 +151,16 @@ __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_
 #pragma unroll
         for (int c = 0; c < 8; c++) acc[jj][c] = 0.0f;
 
-    const uint32_t wbase = wdw_saddr + (uint32_t)c_glob * 2;
 #pragma unroll
     for (int i = 0; i < KS; i++) {
         uint4 w[KS];
 #pragma unroll
-        for (int t = 0; t < KS; t++) w[t] = lds128(wbase + (uint32_t)(i * KS + t) * tap_stride);
-        const uint32_t rbase = stage_saddr + (uint32_t)(r * S + i) * row_bytes +
-                               (uint32_t)(oc0 * S) * px_bytes + (uint32_t)v * 16;
+        for (int t = 0; t < KS; t++)
+            w[t] = *reinterpret_cast<const uint4 *>(wb + (uint32_t)(i * KS + t) * tap_bytes);
+        const uint8_t *xr = xb + (uint32_t)i * row_bytes;
 #pragma unroll
         for (int q = 0; q < (kR - 1) * S + KS; q++) {
-            const uint4 x = lds128(rbase + (uint32_t)q * px_bytes);
+            const uint4 x = *reinterpret_cast<const uint4 *>(xr + (uint32_t)q * px_bytes);
 #pragma unroll
             for (int jj = 0; jj < kR; jj++) {
                 const int t = q - jj * S;
@@ -151,20 +179,22 @@ __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_
     const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
     const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
     const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
+    // A-tile address of (row, c_glob): 64-channel block, 128-byte row, swizzled 16-byte chunk
+    const uint32_t a_blk = a_saddr + (uint32_t)(c_glob >> 6) * (kTileM * 128u);
+    const uint32_t a_chunk = (uint32_t)(c_glob >> 3) & 7u;
 #pragma unroll
     for (int jj = 0; jj < kR; jj++) {
-        const int oc = oc0 + jj;
-        if (oc >= a.tile_w) break;
+        if (jj >= g.nvalid) break;
         uint32_t pk[4];
 #pragma unroll
         for (int c = 0; c < 4; c++)
-            pk[c] = Pack2<T>::run(fmaf(sc[2 * c], acc[jj][2 * c], bi[2 * c]),
-                                  fmaf(sc[2 * c + 1], acc[jj][2 * c + 1], bi[2 * c + 1]), a.act1);
+            pk[c] = Pack2<T>::template run<ACT>(fmaf(sc[2 * c], acc[jj][2 * c], bi[2 * c]),
+                                                fmaf(sc[2 * c + 1], acc[jj][2 * c + 1], bi[2 * c + 1]));
         if (MODE == FUSED) {
-            const int m_row = r * a.tile_w + oc;
-            sts128(a_saddr + sw128_offset(m_row, c_glob, kTileM, 2), pk[0], pk[1], pk[2], pk[3]);
+            const uint32_t m_row = (uint32_t)(g.m_row0 + jj);
+            sts128(a_blk + m_row * 128u + ((a_chunk ^ (m_row & 7u)) << 4), pk[0], pk[1], pk[2], pk[3]);
         } else {
-            const int ho = ho0 + r, wo = wo0 + oc;
+            const int ho = ho0 + g.r, wo = wo0 + g.oc0 + jj;
             if (ho < a.Ho && wo < a.Wo) {
                 T *dst = static_cast<T *>(a.out) +
                          (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
@@ -174,10 +204,15 @@ __device__ __forceinline__ void dw_unit(const Args &a, int u, int chunk, uint32_
     }
 }
 
-__device__ __forceinline__ void tile_coords(const Args &a, long long t, int &n, int &ho0,
-                                            int &wo0) {
-    n = (int)(t / a.tiles_per_img);
-    int rem = (int)(t % a.tiles_per_img);
+// Byte offset of the 16-wide K step k16 in a K-major operand of `rows` rows stored as 64-wide
+// K blocks of 128-byte swizzled rows.
+__device__ __forceinline__ uint32_t k16_offset(int k16, int rows) {
+    return (uint32_t)(k16 >> 2) * (uint32_t)rows * 128u + (uint32_t)(k16 & 3) * 32u;
+}
+
+__device__ __forceinline__ void tile_coords(const Args &a, int t, int &n, int &ho0, int &wo0) {
+    n = t / a.tiles_per_img;
+    const int rem = t - n * a.tiles_per_img;
     ho0 = (rem / a.tiles_w) * a.tile_h;
     wo0 = (rem % a.tiles_w) * a.tile_w;
 }
@@ -194,7 +229,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
     const bool has_mma = MODE != DWONLY;
     const bool has_dw = MODE != PWONLY;
 
-    uint4 *wdw_s = reinterpret_cast<uint4 *>(base_g + a.off_wdw);
+    uint4 *wdw_s = reinterpret_cast<uint4 *>(base_g + a.off_wdw);   // filled in the prologue
     float *sb_s = reinterpret_cast<float *>(base_g + a.off_sb);
     float *s1_s = sb_s, *b1_s = sb_s + a.C, *s2_s = sb_s + 2 * a.C, *b2_s = sb_s + 2 * a.C + a.K;
     const uint32_t bar_base = base_s + a.off_bar;
@@ -246,8 +281,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
 
     if (warp == 0) {
         // ===================================================== TMA producer
-        int issued_per_stage[kMaxStages];
-        for (int s = 0; s < kMaxStages; s++) issued_per_stage[s] = 0;
         bool ok = true;
         if (has_mma && lane == 0) {
             mbar_arrive_expect_tx(bars.wbar, a.wp_img_bytes);
@@ -255,7 +288,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
         }
         if (lane == 0) tma_prefetch_desc(&a.tmap);
         int it = 0;
-        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
+        for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
             int n = 0, ho0 = 0, wo0 = 0;
             if (MODE != PWONLY) tile_coords(a, t, n, ho0, wo0);
             const int nloads = MODE == PWONLY ? 1 : a.nchunks;
@@ -279,17 +312,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
                                     wo0 * S - a.pad, ho0 * S - a.pad, n);
                     }
                 }
-                issued_per_stage[s]++;
                 __syncwarp();
             }
         }
         if (!ok) {
-            // drain: every copy this warp issued lands before the CTA exits
+            // drain: every copy this warp issued lands before the CTA exits (`it` loads were
+            // issued, load i into stage i % stages)
             volatile int no_abort = 0;
-            for (int s = 0; s < a.stages; s++)
-                if (issued_per_stage[s] > 0)
-                    mbar_wait(bars.full + 8 * s, (uint32_t)(issued_per_stage[s] - 1) & 1u,
-                              &no_abort, a.err, lim);
+            for (int s = 0; s < a.stages && s < it; s++) {
+                const int issued = (it - 1 - s) / a.stages + 1;
+                mbar_wait(bars.full + 8 * s, (uint32_t)(issued - 1) & 1u, &no_abort, a.err, lim);
+            }
             if (has_mma) mbar_wait(bars.wbar, 0, &no_abort, a.err, lim);
         }
     } else if (warp == 1 && has_mma) {
@@ -298,7 +331,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
         const uint32_t b_s = base_s + a.off_b;
         const int kb_rows_b = a.K;   // rows of each 64-wide K block of B
         int lt = 0, it = 0;
-        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
+        for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
             const int ab = lt & 1;
             if (!mbar_wait(bars.accempty + 8 * ab, ((uint32_t)(lt >> 1) & 1u) ^ 1u, abort_flag,
                            a.err, lim)) {
@@ -318,21 +351,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
                 tc_fence_after();
                 const uint32_t a_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
                 if (lane == 0) {
-                    for (int k16 = 0; k16 < a.C / 16; k16++) {
-                        const uint32_t koff = (uint32_t)(k16 & 3) * 32u;
-                        const uint64_t ad = sw128_kmajor_desc(a_s + (uint32_t)(k16 >> 2) * kTileM * 128 + koff);
-                        const uint64_t bd = sw128_kmajor_desc(b_s + (uint32_t)(k16 >> 2) * kb_rows_b * 128 + koff);
-                        mma_f16(d_tmem, ad, bd, a.idesc, k16 > 0 ? 1u : 0u);
-                    }
+                    const uint64_t a0 = sw128_kmajor_desc(a_s), b0 = sw128_kmajor_desc(b_s);
+                    for (int k16 = 0; k16 < a.C / 16; k16++)
+                        mma_f16(d_tmem, desc_advance(a0, k16_offset(k16, kTileM)),
+                                desc_advance(b0, k16_offset(k16, kb_rows_b)), a.idesc, k16 > 0 ? 1u : 0u);
                     mma_commit(bars.empty + 8 * s);
                     mma_commit(bars.accfull + 8 * ab);
                 }
                 __syncwarp();
             } else {
+                // one A tile: chunk j of tile lt is its (lt+1)-th fill
+                const uint32_t apar = (uint32_t)lt & 1u;
                 const uint32_t a_s = base_s + a.off_a;
+                const uint32_t afull_b = bars.afull, aempty_b = bars.aempty;
+                const uint64_t a_desc0 = sw128_kmajor_desc(a_s), b_desc0 = sw128_kmajor_desc(b_s);
                 const int k16_per_chunk = a.chunk_c / 16;
                 for (int j = 0; j < a.nchunks; j++) {
-                    if (!mbar_wait(bars.afull + 8 * j, (uint32_t)lt & 1u, abort_flag, a.err, lim)) {
+                    if (!mbar_wait(afull_b + 8 * j, apar, abort_flag, a.err, lim)) {
                         ok = false;
                         break;
                     }
@@ -340,12 +375,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
                     if (lane == 0) {
                         for (int kk = 0; kk < k16_per_chunk; kk++) {
                             const int k16 = j * k16_per_chunk + kk;
-                            const uint32_t koff = (uint32_t)(k16 & 3) * 32u;
-                            const uint64_t ad = sw128_kmajor_desc(a_s + (uint32_t)(k16 >> 2) * kTileM * 128 + koff);
-                            const uint64_t bd = sw128_kmajor_desc(b_s + (uint32_t)(k16 >> 2) * kb_rows_b * 128 + koff);
-                            mma_f16(d_tmem, ad, bd, a.idesc, k16 > 0 ? 1u : 0u);
+                            mma_f16(d_tmem, desc_advance(a_desc0, k16_offset(k16, kTileM)),
+                                    desc_advance(b_desc0, k16_offset(k16, kb_rows_b)), a.idesc,
+                                    k16 > 0 ? 1u : 0u);
                         }
-                        mma_commit(bars.aempty + 8 * j);
+                        mma_commit(aempty_b + 8 * j);
                     }
                     __syncwarp();
                 }
@@ -363,101 +397,132 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
     } else if (warp >= 2 && warp < 2 + kEpiWarps && has_mma) {
         // ===================================================== epilogue
         // TMEM -> registers -> scale/bias/act -> 16-bit -> 128B-swizzled staging tile in shared
-        // memory -> one TMA tensor store per 64-channel block (full lines, clipped at the edges)
+        // memory -> one TMA tensor store per 64-channel block (full lines, clipped at the edges).
+        // (Splitting the stores per block so that they overlap the next block's math measured
+        // slower: more barriers and proxy fences per tile.)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const bool issuer = warp == 2 && lane == 0;
-        const uint32_t out_s = base_s + a.off_out;
         const int nkb_out = (a.K + 63) / 64;
         const uint32_t swz = (uint32_t)(row & 7);
-        const uint32_t row_s = out_s + (uint32_t)row * 128;
-        int lt = 0;
-        for (long long t = blockIdx.x; t < a.num_tiles; t += gridDim.x, lt++) {
-            const int ab = lt & 1;
-            const bool ok =
-                mbar_wait(bars.accfull + 8 * ab, (uint32_t)(lt >> 1) & 1u, abort_flag, a.err, lim);
-            if (issuer) bulk_wait_group_read<0>();   // staging free: the last store has read it
-            if (named_barrier_or(1, 32 * kEpiWarps, !ok)) break;
-            tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
-            for (int c0 = 0; c0 < a.K; c0 += 16) {
-                uint32_t rr[16];
-                tmem_ld16(taddr + (uint32_t)c0, rr);
-                tmem_ld_wait();
+        uint32_t out_s = base_s + a.off_out, row_s = out_s + (uint32_t)row * 128;
+        with_act(a.act2, [&](auto act_tag) {
+            constexpr int ACT = decltype(act_tag)::value;
+            // scale/bias/act on 16 accumulator columns starting at c0, rounded and written to the
+            // swizzled staging row
+            auto emit16 = [&](const uint32_t (&rr)[16], int c0) {
                 uint32_t pk[8];
 #pragma unroll
                 for (int i4 = 0; i4 < 4; i4++) {
                     const float4 sc = *reinterpret_cast<const float4 *>(s2_s + c0 + 4 * i4);
                     const float4 bi = *reinterpret_cast<const float4 *>(b2_s + c0 + 4 * i4);
-                    pk[2 * i4] = Pack2<T>::run(fmaf(sc.x, __uint_as_float(rr[4 * i4]), bi.x),
-                                               fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y),
-                                               a.act2);
-                    pk[2 * i4 + 1] =
-                        Pack2<T>::run(fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z),
-                                      fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w), a.act2);
+                    const float y0 = fmaf(sc.x, __uint_as_float(rr[4 * i4]), bi.x);
+                    const float y1 = fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y);
+                    const float y2 = fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z);
+                    const float y3 = fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w);
+                    pk[2 * i4] = Pack2<T>::template run<ACT>(y0, y1);
+                    pk[2 * i4 + 1] = Pack2<T>::template run<ACT>(y2, y3);
                 }
                 const uint32_t blk = (uint32_t)(c0 >> 6) * kOutBlock;
                 const uint32_t ch = (uint32_t)((c0 & 63) >> 3);
                 sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
                 sts128(row_s + blk + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.accempty + 8 * ab);   // TMEM buffer may be reused
-            fence_proxy_async_smem();                              // staging visible to the TMA
-            named_barrier(1, 32 * kEpiWarps);
-            if (issuer) {
-                if (MODE == PWONLY) {
-                    for (int kb = 0; kb < nkb_out; kb++)
-                        tma_store_2d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
-                                     (int)(t * kTileM));
-                } else {
-                    int n, ho0, wo0;
-                    tile_coords(a, t, n, ho0, wo0);
-                    for (int kb = 0; kb < nkb_out; kb++)
-                        tma_store_4d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64, wo0,
-                                     ho0, n);
+            };
+            int lt = 0;
+            for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, lt++) {
+                const int ab = lt & 1;
+                const bool ok = mbar_wait(bars.accfull + 8 * ab, (uint32_t)(lt >> 1) & 1u,
+                                          abort_flag, a.err, lim);
+                // this tile's staging buffer is free once the stores that last read it are done
+                // reading (with two buffers the previous tile's stores may still be running)
+                if (issuer) {
+                    if (a.out_bufs == 2)
+                        bulk_wait_group_read<1>();
+                    else
+                        bulk_wait_group_read<0>();
                 }
-                bulk_commit_group();
+                if (named_barrier_or(1, 32 * kEpiWarps, !ok)) break;
+                out_s = base_s + a.off_out + (uint32_t)(a.out_bufs == 2 ? (lt & 1) : 0) * a.out_buf_bytes;
+                row_s = out_s + (uint32_t)row * 128;
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
+                // (K is a multiple of 16.  Keeping the next load in flight while converting the
+                // current columns measured slower.)
+                for (int c0 = 0; c0 < a.K; c0 += 16) {
+                    uint32_t rr[16];
+                    tmem_ld16(taddr + (uint32_t)c0, rr);
+                    tmem_ld_wait();
+                    emit16(rr, c0);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.accempty + 8 * ab);   // TMEM buffer reusable
+                fence_proxy_async_smem();                              // staging visible to TMA
+                named_barrier(1, 32 * kEpiWarps);
+                if (issuer) {
+                    if (MODE == PWONLY) {
+                        for (int kb = 0; kb < nkb_out; kb++)
+                            tma_store_2d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
+                                         t * kTileM);
+                    } else {
+                        int n, ho0, wo0;
+                        tile_coords(a, t, n, ho0, wo0);
+                        for (int kb = 0; kb < nkb_out; kb++)
+                            tma_store_4d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
+                                     wo0, ho0, n);
+                    }
+                    bulk_commit_group();
+                }
             }
-        }
+        });
         if (issuer) bulk_wait_group<0>();
     } else if (warp >= kFirstDwWarp && has_dw) {
         // ===================================================== DW warps
         const int tid = (warp - kFirstDwWarp) * 32 + lane;
         const int nthr = a.n_dw_warps * 32;
         const int units = a.tile_h * a.ngroups * (a.chunk_c >> 3);
-        const uint32_t a_s = base_s + a.off_a;
-        int lt = 0, it = 0;
-        bool ok = true;
-        for (long long t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
-            int n, ho0, wo0;
-            tile_coords(a, t, n, ho0, wo0);
-            for (int j = 0; j < a.nchunks; j++, it++) {
-                const int s = it % a.stages;
-                const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-                if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                if (MODE == FUSED &&
-                    !mbar_wait(bars.aempty + 8 * j, ((uint32_t)lt & 1u) ^ 1u, abort_flag, a.err, lim)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t stage_s = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
-                for (int u = tid; u < units; u += nthr)
-                    dw_unit<T, KS, S, MODE>(a, u, j, stage_s, base_s + a.off_wdw, s1_s, b1_s, a_s, n,
-                                            ho0, wo0);
-                if (MODE == FUSED) fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bars.empty + 8 * s);
-                    if (MODE == FUSED) mbar_arrive(bars.afull + 8 * j);
+        with_act(a.act1, [&](auto act_tag) {
+            constexpr int ACT = decltype(act_tag)::value;
+            const uint8_t *wdw_g = base_g + a.off_wdw;
+            // the thread's first unit (most plans give each thread at most one per chunk)
+            const DwUnit g0 = dw_unit_geom<S>(a, tid < units ? tid : 0);
+            int lt = 0, it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
+                int n, ho0, wo0;
+                tile_coords(a, t, n, ho0, wo0);
+                const uint32_t apar = (uint32_t)lt & 1u;
+                const uint32_t a_s = base_s + a.off_a;
+                const uint32_t afull_b = bars.afull, aempty_b = bars.aempty;
+                for (int j = 0; j < a.nchunks; j++, it++) {
+                    const int s = it % a.stages;
+                    const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+                    if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    if (MODE == FUSED &&
+                        !mbar_wait(aempty_b + 8 * j, apar ^ 1u, abort_flag, a.err, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
+                    if (tid < units)
+                        dw_unit<T, KS, S, MODE, ACT>(a, g0, j, stage_g, wdw_g, s1_s, b1_s, a_s, n,
+                                                     ho0, wo0);
+                    for (int u = tid + nthr; u < units; u += nthr)
+                        dw_unit<T, KS, S, MODE, ACT>(a, dw_unit_geom<S>(a, u), j, stage_g, wdw_g,
+                                                     s1_s, b1_s, a_s, n, ho0, wo0);
+                    if (MODE == FUSED) fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bars.empty + 8 * s);
+                        if (MODE == FUSED) mbar_arrive(afull_b + 8 * j);
+                    }
                 }
             }
-        }
+        });
     }
 
     __syncwarp();
@@ -502,12 +567,14 @@ struct Layout {
     int stages;
 };
 
-Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int smem_cap) {
+Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int smem_cap,
+                   int out_bufs) {
     Layout L{};
     const int C = cm, K = d->k_out, nkb = (C + 63) / 64;
     const uint32_t b_bytes = mode == DWONLY ? 0u : (uint32_t)nkb * K * 128;
     const uint32_t a_bytes = mode == FUSED ? (uint32_t)nkb * kTileM * 128 : 0u;
-    const uint32_t out_bytes = mode == DWONLY ? 0u : (uint32_t)((K + 63) / 64) * kOutBlock;
+    const uint32_t out_bytes =
+        mode == DWONLY ? 0u : (uint32_t)(out_bufs * ((K + 63) / 64)) * kOutBlock;
     L.off_b = 0;
     L.off_a = align_up(b_bytes, 1024);
     L.off_out = align_up(L.off_a + a_bytes, 1024);
@@ -586,7 +653,13 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
                 t.chunk_c = chunk;
                 t.nchunks = C / chunk;
                 t.stages = kMaxStages;
-                Layout L = make_layout(d, t, cm, FUSED, smem_cap);
+                // two output staging tiles when that still leaves three input stages
+                Layout L = make_layout(d, t, cm, FUSED, smem_cap, 2);
+                t.out_bufs = 2;
+                if (L.stages < 3) {
+                    L = make_layout(d, t, cm, FUSED, smem_cap, 1);
+                    t.out_bufs = 1;
+                }
                 if (L.stages < 2) continue;
                 t.stages = L.stages;
                 t.smem_bytes = (int)L.total;
@@ -682,7 +755,8 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     const TcPlan &p = h->tc;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    Layout L = make_layout(&d, p, h->cm, mode, h->smem_optin);
+    const int out_bufs = mode == FUSED ? p.out_bufs : 1;
+    Layout L = make_layout(&d, p, h->cm, mode, h->smem_optin, out_bufs);
     if (L.stages < 1) return cudaErrorInvalidConfiguration;
     Args a;
     memset(&a, 0, sizeof(a));
@@ -699,7 +773,8 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         a.P = P;
-        a.num_tiles = (P + kTileM - 1) / kTileM;
+        if (P > (long long)INT_MAX - kTileM) return cudaErrorInvalidValue;   // 32-bit TMA coordinates
+        a.num_tiles = (int)((P + kTileM - 1) / kTileM);
     } else {
         cuuint64_t gdim[4] = {(cuuint64_t)d.c, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
         cuuint64_t gstride[3] = {(cuuint64_t)d.c * 2, (cuuint64_t)d.w * d.c * 2,
@@ -709,7 +784,8 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
         cr = enc(&a.tmap, dt, 4, const_cast<void *>(in), gdim, gstride, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        a.num_tiles = p.num_tiles;
+        if (p.num_tiles > INT_MAX) return cudaErrorInvalidValue;
+        a.num_tiles = (int)p.num_tiles;
     }
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (mode == PWONLY) {
@@ -764,6 +840,8 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.off_b = L.off_b;
     a.off_a = L.off_a;
     a.off_out = L.off_out;
+    a.out_bufs = out_bufs;
+    a.out_buf_bytes = (uint32_t)((d.k_out + 63) / 64) * kOutBlock;
     a.off_in = L.off_in;
     a.off_wdw = L.off_wdw;
     a.off_sb = L.off_sb;
