@@ -28,6 +28,7 @@ struct TcPlan {
     int ctas = 0;
     int tmem_cols = 0;
     int out_bufs = 1;             // DW->PW output staging tiles (2: stores overlap the next tile)
+    int dw_per_chunk = 0;         // >0: each DW warp serves one channel chunk (taps in registers)
 };
 
 struct fcm_handle {

@@ -42,6 +42,10 @@ constexpr int kEpiWarps = 4;
 constexpr int kFirstDwWarp = 2 + kEpiWarps;
 constexpr int kMaxDwWarps = 10;   // 16 warps in all: up to 128 registers a thread
 constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);
+// Chunk-bound DW warps (each warp serves one channel chunk and keeps its taps in registers):
+// up to 14 DW warps, 20 in all, 96 registers a thread.
+constexpr int kMaxDwWarpsBound = 14;
+constexpr int kMaxThreadsBound = 32 * (kFirstDwWarp + kMaxDwWarpsBound);
 constexpr int kR = 4;          // output pixels per DW work unit (along W)
 constexpr int kTileM = 128;    // MMA M: pixels per output tile (padded)
 constexpr int kMaxStages = 8;
@@ -64,6 +68,7 @@ struct Args {
     int tile_h, tile_w, tiles_w, tiles_per_img, ngroups;
     int in_rows, in_cols;
     int chunk_c, nchunks, stages, n_dw_warps;
+    int dw_per_chunk;          // chunk-bound DW warps per chunk (0: every DW warp serves every chunk)
     int act1, act2;
     uint32_t tmem_cols, idesc, wp_img_bytes, in_stage_bytes;
     uint32_t off_b, off_a, off_in, in_stage_stride, off_out, off_wdw, off_sb, off_bar;
@@ -133,11 +138,12 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
 // (fma.rn.f32.{f16,bf16}).  `stage` and `wdw` are shared-memory pointers; the loads are plain
 // C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
 // which clobber memory).
-template <typename T, int KS, int S, int MODE, int ACT>
+template <typename T, int KS, int S, int MODE, int ACT, bool RT>
 __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chunk,
                                         const uint8_t *stage, const uint8_t *wdw,
-                                        const float *s1_s, const float *b1_s, uint32_t a_saddr,
-                                        int n, int ho0, int wo0) {
+                                        const uint4 (&wreg)[KS * KS], const float *s1_s,
+                                        const float *b1_s, uint32_t a_saddr, int n, int ho0,
+                                        int wo0) {
     const int c_glob = chunk * a.chunk_c + g.cv;
     const uint32_t px_bytes = (uint32_t)a.chunk_c * 2u;
     const uint32_t row_bytes = (uint32_t)a.in_cols * px_bytes;
@@ -156,7 +162,8 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
         uint4 w[KS];
 #pragma unroll
         for (int t = 0; t < KS; t++)
-            w[t] = *reinterpret_cast<const uint4 *>(wb + (uint32_t)(i * KS + t) * tap_bytes);
+            w[t] = RT ? wreg[i * KS + t]
+                      : *reinterpret_cast<const uint4 *>(wb + (uint32_t)(i * KS + t) * tap_bytes);
         const uint8_t *xr = xb + (uint32_t)i * row_bytes;
 #pragma unroll
         for (int q = 0; q < (kR - 1) * S + KS; q++) {
@@ -217,8 +224,10 @@ __device__ __forceinline__ void tile_coords(const Args &a, int t, int &n, int &h
     wo0 = (rem % a.tiles_w) * a.tile_w;
 }
 
-template <typename T, int KS, int S, int MODE>
-__global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_constant__ Args a) {
+// DWB: chunk-bound DW warps (Args::dw_per_chunk > 0), with their own register budget.
+template <typename T, int KS, int S, int MODE, int DWB>
+__global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
+    dwpw_kernel(const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -253,11 +262,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; s++) {
             mbar_init(bars.full + 8 * s, 1);
-            mbar_init(bars.empty + 8 * s, MODE == PWONLY ? 1 : a.n_dw_warps);
+            mbar_init(bars.empty + 8 * s, MODE == PWONLY ? 1 : DWB ? a.dw_per_chunk : a.n_dw_warps);
         }
         if (MODE == FUSED) {
             for (int j = 0; j < a.nchunks; j++) {
-                mbar_init(bars.afull + 8 * j, a.n_dw_warps);
+                mbar_init(bars.afull + 8 * j, DWB ? a.dw_per_chunk : a.n_dw_warps);
                 mbar_init(bars.aempty + 8 * j, 1);
             }
         }
@@ -447,13 +456,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
-                // (K is a multiple of 16.  Keeping the next load in flight while converting the
-                // current columns measured slower.)
-                for (int c0 = 0; c0 < a.K; c0 += 16) {
-                    uint32_t rr[16];
-                    tmem_ld16(taddr + (uint32_t)c0, rr);
+                // two loads of 16 columns, one wait (K is a multiple of 16; keeping a load in
+                // flight across the conversion measured slower)
+                for (int c0 = 0; c0 < a.K; c0 += 32) {
+                    uint32_t ra[16], rb[16];
+                    const bool two = c0 + 16 < a.K;
+                    tmem_ld16(taddr + (uint32_t)c0, ra);
+                    if (two) tmem_ld16(taddr + (uint32_t)(c0 + 16), rb);
                     tmem_ld_wait();
-                    emit16(rr, c0);
+                    emit16(ra, c0);
+                    if (two) emit16(rb, c0 + 16);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -479,50 +491,94 @@ __global__ void __launch_bounds__(kMaxThreads, 1) dwpw_kernel(const __grid_const
         if (issuer) bulk_wait_group<0>();
     } else if (warp >= kFirstDwWarp && has_dw) {
         // ===================================================== DW warps
-        const int tid = (warp - kFirstDwWarp) * 32 + lane;
-        const int nthr = a.n_dw_warps * 32;
         const int units = a.tile_h * a.ngroups * (a.chunk_c >> 3);
-        with_act(a.act1, [&](auto act_tag) {
-            constexpr int ACT = decltype(act_tag)::value;
-            const uint8_t *wdw_g = base_g + a.off_wdw;
-            // the thread's first unit (most plans give each thread at most one per chunk)
-            const DwUnit g0 = dw_unit_geom<S>(a, tid < units ? tid : 0);
-            int lt = 0, it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
-                int n, ho0, wo0;
-                tile_coords(a, t, n, ho0, wo0);
-                const uint32_t apar = (uint32_t)lt & 1u;
-                const uint32_t a_s = base_s + a.off_a;
-                const uint32_t afull_b = bars.afull, aempty_b = bars.aempty;
-                for (int j = 0; j < a.nchunks; j++, it++) {
+        const uint8_t *wdw_g = base_g + a.off_wdw;
+        const uint32_t a_s = base_s + a.off_a;
+        if (DWB) {
+            // Chunk-bound: warp w serves chunk w / dw_per_chunk of every tile, one unit per
+            // thread (the planner guarantees units <= 32 * dw_per_chunk), with the unit's taps
+            // held in registers for the whole kernel.
+            const int dw_w = warp - kFirstDwWarp;
+            const int jm = dw_w / a.dw_per_chunk;
+            const int tid = (dw_w % a.dw_per_chunk) * 32 + lane;
+            const bool has_unit = tid < units;
+            const DwUnit g0 = dw_unit_geom<S>(a, has_unit ? tid : 0);
+            uint4 wreg[KS * KS];
+            {
+                const uint8_t *wb = wdw_g + (uint32_t)(jm * a.chunk_c + g0.cv) * 2u;
+#pragma unroll
+                for (int t = 0; t < KS * KS; t++)
+                    wreg[t] = *reinterpret_cast<const uint4 *>(wb + (uint32_t)t * (uint32_t)a.C * 2u);
+            }
+            with_act(a.act1, [&](auto act_tag) {
+                constexpr int ACT = decltype(act_tag)::value;
+                int lt = 0;
+                for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, lt++) {
+                    int n, ho0, wo0;
+                    tile_coords(a, t, n, ho0, wo0);
+                    const int it = lt * a.nchunks + jm;   // the producer's load index of this chunk
                     const int s = it % a.stages;
                     const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-                    if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
-                        ok = false;
+                    if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) break;
+                    if (MODE == FUSED && !mbar_wait(bars.aempty + 8 * jm, ((uint32_t)lt & 1u) ^ 1u,
+                                                    abort_flag, a.err, lim))
                         break;
-                    }
-                    if (MODE == FUSED &&
-                        !mbar_wait(aempty_b + 8 * j, apar ^ 1u, abort_flag, a.err, lim)) {
-                        ok = false;
-                        break;
-                    }
                     const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
-                    if (tid < units)
-                        dw_unit<T, KS, S, MODE, ACT>(a, g0, j, stage_g, wdw_g, s1_s, b1_s, a_s, n,
-                                                     ho0, wo0);
-                    for (int u = tid + nthr; u < units; u += nthr)
-                        dw_unit<T, KS, S, MODE, ACT>(a, dw_unit_geom<S>(a, u), j, stage_g, wdw_g,
-                                                     s1_s, b1_s, a_s, n, ho0, wo0);
+                    if (has_unit)
+                        dw_unit<T, KS, S, MODE, ACT, true>(a, g0, jm, stage_g, wdw_g, wreg, s1_s,
+                                                           b1_s, a_s, n, ho0, wo0);
                     if (MODE == FUSED) fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(bars.empty + 8 * s);
-                        if (MODE == FUSED) mbar_arrive(afull_b + 8 * j);
+                        if (MODE == FUSED) mbar_arrive(bars.afull + 8 * jm);
                     }
                 }
-            }
-        });
+            });
+        } else {
+            // Every DW warp serves every chunk; taps are read from shared memory.
+            const int tid = (warp - kFirstDwWarp) * 32 + lane;
+            const int nthr = a.n_dw_warps * 32;
+            const uint4 wnone[KS * KS] = {};
+            // the thread's first unit (most plans give each thread at most one per chunk)
+            const DwUnit g0 = dw_unit_geom<S>(a, tid < units ? tid : 0);
+            with_act(a.act1, [&](auto act_tag) {
+                constexpr int ACT = decltype(act_tag)::value;
+                int lt = 0, it = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x, lt++) {
+                    int n, ho0, wo0;
+                    tile_coords(a, t, n, ho0, wo0);
+                    for (int j = 0; j < a.nchunks; j++, it++) {
+                        const int s = it % a.stages;
+                        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+                        if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        if (MODE == FUSED && !mbar_wait(bars.aempty + 8 * j, ((uint32_t)lt & 1u) ^ 1u,
+                                                        abort_flag, a.err, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
+                        if (tid < units)
+                            dw_unit<T, KS, S, MODE, ACT, false>(a, g0, j, stage_g, wdw_g, wnone, s1_s,
+                                                                b1_s, a_s, n, ho0, wo0);
+                        for (int u = tid + nthr; u < units; u += nthr)
+                            dw_unit<T, KS, S, MODE, ACT, false>(a, dw_unit_geom<S>(a, u), j, stage_g,
+                                                                wdw_g, wnone, s1_s, b1_s, a_s, n,
+                                                                ho0, wo0);
+                        if (MODE == FUSED) fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(bars.empty + 8 * s);
+                            if (MODE == FUSED) mbar_arrive(bars.afull + 8 * j);
+                        }
+                    }
+                }
+            });
+        }
     }
 
     __syncwarp();
@@ -680,6 +736,16 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
                 }
                 t.threads = 32 * (kFirstDwWarp + best_w);
                 t.dw_warps = best_w;
+                t.dw_per_chunk = 0;
+                // chunk-bound DW warps (taps in registers) when the taps fit (k <= 3), one unit
+                // per thread, and at most kMaxDwWarpsBound warps
+                const int wpc = (units + 31) / 32;
+                if (KS <= 3 && wpc * t.nchunks <= kMaxDwWarpsBound) {
+                    t.dw_per_chunk = wpc;
+                    t.dw_warps = wpc * t.nchunks;
+                    t.threads = 32 * (kFirstDwWarp + t.dw_warps);
+                    best_eff = (double)units / (32.0 * wpc);
+                }
                 t.ctas = (int)std::min<long long>(t.num_tiles, num_sms);
                 t.tmem_cols = (int)pow2_cols(2 * d->k_out);
                 // score: pixels per tile (MMA/halo efficiency) x thread efficiency x pipeline
@@ -729,13 +795,21 @@ fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_hos
 
 namespace {
 
-template <typename T, int KS, int S, int MODE>
-cudaError_t launch_t(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
-    auto k = dwpw_kernel<T, KS, S, MODE>;
+template <typename T, int KS, int S, int MODE, int DWB>
+cudaError_t launch_k(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
+    auto k = dwpw_kernel<T, KS, S, MODE, DWB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<ctas, threads, smem, st>>>(a);
     return cudaGetLastError();
+}
+
+template <typename T, int KS, int S, int MODE>
+cudaError_t launch_t(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
+    if constexpr (KS <= 3 && MODE != PWONLY) {
+        if (a.dw_per_chunk > 0) return launch_k<T, KS, S, MODE, 1>(a, ctas, threads, smem, st);
+    }
+    return launch_k<T, KS, S, MODE, 0>(a, ctas, threads, smem, st);
 }
 
 template <typename T, int MODE>
@@ -830,6 +904,7 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.nchunks = p.nchunks;
     a.stages = L.stages;
     a.n_dw_warps = mode == PWONLY ? 0 : p.dw_warps;
+    a.dw_per_chunk = mode == PWONLY ? 0 : p.dw_per_chunk;
     a.act1 = d.act1;
     a.act2 = d.act2;
     a.tmem_cols = (uint32_t)p.tmem_cols;
