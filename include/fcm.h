@@ -188,6 +188,68 @@ FCM_API long long fcm_model_dwpw_gma(long long c, long long overlap, long long d
                              long long pw_ofms_sz, long long ofms_hw, long long ofms_tile_hw,
                              long long dw_weights_sz);
 
+/* Eq. 4: PWDW FCM global memory accesses, as printed. */
+FCM_API long long fcm_model_pwdw_gma(long long pw_ifms_d, long long dw_overlap, long long pw_ifms_sz,
+                             long long pw_weights_sz, long long pw_weights_tile_sz,
+                             long long dw_weights_sz, long long dw_weights_tile_sz,
+                             long long dw_ofms_sz, long long dw_ofms_tile_sz, long long dw_ofms_hw,
+                             long long dw_ofms_tile_hw);
+/* PWPW FCM estimator, built from Eq. 2 the way section IV-B builds Eq. 4 (the first layer's
+ * input is re-read once per weight tile of the second layer, which recomputes the
+ * intermediate; the second layer's output is written once; both layers' weights are read once
+ * per spatial tile):
+ * Pw1IFMsSz * ceil(Pw2WeightsSz/Pw2WeightsTileSz) + Pw2OFMsSz
+ *   + ceil(OFMsHW/OFMsTileHW) * (Pw1WeightsSz + Pw2WeightsSz). */
+FCM_API long long fcm_model_pwpw_gma(long long pw1_ifms_sz, long long pw1_weights_sz,
+                             long long pw2_weights_sz, long long pw2_weights_tile_sz,
+                             long long pw2_ofms_sz, long long ofms_hw, long long ofms_tile_hw);
+
+/* ---- FusePlanner over a chain of layers, section IV ("FusePlanner overview", IV-A, IV-B).
+ * The i-th layer's input is the (i-1)-th layer's output (H, W, C checked).  Each layer's
+ * minimum layer-by-layer estimate (Eq. 3 for DW, Eq. 2 for PW) and each adjacent pair's
+ * minimum FCM estimate (DWPW: fcm_model_dwpw_gma; PWDW: Eq. 4; PWPW: fcm_model_pwpw_gma) are
+ * searched over the tiles that fit in L1 (three tiles for a layer, five for an FCM) and give
+ * at least `num_sms` output tiles over a batch of `batch` images, tile sizes being multiples of
+ * the warp size (pixels per tile, channels per tile; a dimension below 32 is taken whole).
+ * When no such tile reaches `num_sms` output tiles, those with the most tiles are taken and
+ * `tiles_ok` / `fcm_tiles_ok` say so.  A pair is fused when its
+ * FCM estimate is below the sum of its layers' estimates; where candidate pairs share a layer
+ * the decomposition with the smallest chain total is chosen.  No counterpart for DW -> DW. */
+typedef enum { FCM_LAYER_DW = 0, FCM_LAYER_PW = 1 } fcm_layer_kind;
+typedef enum {
+    FCM_MODULE_LBL_DW = 0,       /* this layer runs alone (depthwise) */
+    FCM_MODULE_LBL_PW = 1,       /* this layer runs alone (pointwise) */
+    FCM_MODULE_DWPW = 2,         /* this layer and the next form a DWPW FCM */
+    FCM_MODULE_PWDW = 3,         /* ... a PWDW FCM */
+    FCM_MODULE_PWPW = 4,         /* ... a PWPW FCM */
+    FCM_MODULE_FUSED_SECOND = 5  /* second layer of the FCM chosen for the previous layer */
+} fcm_module_kind;
+typedef struct {
+    int kind;           /* fcm_layer_kind */
+    int h, w, c;        /* input extent and channels */
+    int k_out;          /* PW: filters; DW: 0 or c */
+    int ksize, stride, pad;   /* DW only (a PW layer is 1x1, stride 1, no padding) */
+} fcm_layer;
+typedef struct {
+    int fuse_with_next; /* 1: this layer and the next run as one FCM */
+    int module;         /* fcm_module_kind chosen for this layer */
+    int fcm_module;     /* FCM kind this layer would form with the next (-1: none exists) */
+    int tile_h, tile_w, tile_c;              /* best layer-by-layer OFM tile (pixels, channels) */
+    int fcm_tile_h, fcm_tile_w, fcm_tile_c;  /* best FCM OFM tile with the next layer */
+    int tiles_ok;       /* 1: the layer-by-layer tile gives >= num_sms output tiles */
+    int fcm_tiles_ok;   /* same for the FCM tile */
+    long long gma_lbl;  /* minimum layer-by-layer estimate, elements per image */
+    long long gma_fcm;  /* minimum FCM estimate of this layer and the next, -1 if none */
+} fcm_layer_plan;
+/* `layers[n_layers]` (host memory, read only); `out[n_layers]` (host memory, written);
+ * `total_gma` (optional) receives the chain total of the chosen decomposition.  `l1_bytes` is
+ * the on-chip capacity the tiles must fit in, `elem_bytes` the element size.  Errors:
+ * FCM_ERR_INVALID_ARG for bad or mismatched shapes, FCM_ERR_SMEM_BUDGET when a layer has no
+ * admissible tile.  Host only, no GPU needed. */
+FCM_API fcm_status fcm_fuse_plan(const fcm_layer *layers, int n_layers, int batch,
+                                 int num_sms, long long l1_bytes, int elem_bytes,
+                                 fcm_layer_plan *out, long long *total_gma);
+
 #ifdef __cplusplus
 }
 #endif

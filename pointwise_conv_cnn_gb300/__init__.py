@@ -18,7 +18,9 @@ __all__ = [
     "FCM_OK", "FcmError", "FcmDesc", "FcmPlanInfo", "FusedConvModule", "load_library",
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
-    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "EXPORTED_SYMBOLS",
+    "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_model_pwdw_gma",
+    "fcm_model_pwpw_gma", "fcm_fuse_plan", "FcmLayer", "FcmLayerPlan", "LAYER_KINDS", "MODULES",
+    "EXPORTED_SYMBOLS",
     "fcm_run_unfused_static",
     "DTYPES", "ACTS", "MODES",
 ]
@@ -40,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_run_unfused_static",
+    "fcm_model_pwdw_gma", "fcm_model_pwpw_gma", "fcm_fuse_plan",
 )
 
 
@@ -64,6 +67,29 @@ class FcmPlanInfo(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+LAYER_KINDS = {"dw": 0, "pw": 1}
+MODULES = {0: "lbl_dw", 1: "lbl_pw", 2: "dwpw", 3: "pwdw", 4: "pwpw", 5: "fused_second", -1: None}
+
+
+class FcmLayer(ctypes.Structure):
+    """Mirror of fcm_layer."""
+    _fields_ = [(n, ctypes.c_int) for n in ("kind", "h", "w", "c", "k_out", "ksize", "stride", "pad")]
+
+
+class FcmLayerPlan(ctypes.Structure):
+    """Mirror of fcm_layer_plan."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "fuse_with_next", "module", "fcm_module", "tile_h", "tile_w", "tile_c", "fcm_tile_h",
+        "fcm_tile_w", "fcm_tile_c", "tiles_ok", "fcm_tiles_ok")] + [("gma_lbl", ctypes.c_longlong),
+                                        ("gma_fcm", ctypes.c_longlong)]
+
+    def as_dict(self) -> dict:
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["module"] = MODULES[d["module"]]
+        d["fcm_module"] = MODULES[d["fcm_module"]]
+        return d
 
 
 _lock = threading.Lock()
@@ -104,9 +130,14 @@ def load_library(path: str | None = None):
         lib.fcm_model_pw_gma.argtypes = [ll] * 5
         lib.fcm_model_dw_gma.argtypes = [ll] * 7
         lib.fcm_model_dwpw_gma.argtypes = [ll] * 9
+        lib.fcm_model_pwdw_gma.argtypes = [ll] * 11
+        lib.fcm_model_pwpw_gma.argtypes = [ll] * 7
         for f in ("fcm_model_overlap", "fcm_model_pw_gma", "fcm_model_dw_gma",
-                  "fcm_model_dwpw_gma"):
+                  "fcm_model_dwpw_gma", "fcm_model_pwdw_gma", "fcm_model_pwpw_gma"):
             getattr(lib, f).restype = ll
+        lib.fcm_fuse_plan.argtypes = [ctypes.POINTER(FcmLayer), i, i, i, ll, i,
+                                      ctypes.POINTER(FcmLayerPlan), ctypes.POINTER(ll)]
+        lib.fcm_fuse_plan.restype = i
         del fp
         _lib = lib
         return lib
@@ -200,6 +231,31 @@ def fcm_model_dw_gma(*a) -> int:
 
 def fcm_model_dwpw_gma(*a) -> int:
     return load_library().fcm_model_dwpw_gma(*a)
+
+
+def fcm_model_pwdw_gma(*a) -> int:
+    return load_library().fcm_model_pwdw_gma(*a)
+
+
+def fcm_model_pwpw_gma(*a) -> int:
+    return load_library().fcm_model_pwpw_gma(*a)
+
+
+def fcm_fuse_plan(layers, batch: int = 1, num_sms: int = 152, l1_bytes: int = 232448,
+                  elem_bytes: int = 2) -> tuple[list[dict], int]:
+    """FusePlanner over a chain of layers.  Each layer is a dict with kind ("dw" or "pw"),
+    h, w, c, and k_out (PW) or ksize/stride/pad (DW).  Returns the per-layer plans and the
+    chain total (elements per image)."""
+    n = len(layers)
+    arr = (FcmLayer * n)()
+    for i, L in enumerate(layers):
+        arr[i] = FcmLayer(LAYER_KINDS[L["kind"]], L["h"], L["w"], L["c"], L.get("k_out", 0),
+                          L.get("ksize", 1), L.get("stride", 1), L.get("pad", 0))
+    out = (FcmLayerPlan * n)()
+    total = ctypes.c_longlong()
+    _check(load_library().fcm_fuse_plan(arr, n, batch, num_sms, l1_bytes, elem_bytes, out,
+                                        ctypes.byref(total)))
+    return [o.as_dict() for o in out], total.value
 
 
 class FusedConvModule:

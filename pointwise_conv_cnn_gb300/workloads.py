@@ -195,6 +195,9 @@ WORKLOADS = (
              "normal"),
     Workload("b2b_dense3x3_f16", 64, 56, 56, 64, 64, "dense", 3, 1, 1, "relu", "relu", "f16",
              "normal", mid=64),
+    # two 1x1 convolutions back to back (the PWPW pair): 64 -> 128 (ReLU6) -> 64 (linear)
+    Workload("pwpw_f16", 64, 56, 56, 64, 64, "dense", 1, 1, 0, "relu6", "none", "f16", "normal",
+             mid=128),
 )
 BY_NAME = {w.name: w for w in WORKLOADS}
 
