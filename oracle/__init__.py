@@ -10,8 +10,9 @@ file with gcc, loads it with ctypes and marshals numpy arrays.  Inputs of any fl
 upcast to float64 exactly before the call; outputs are float64.
 
 Definitions followed (see the C file for the full list): "Fusing Depthwise and Pointwise
-Convolutions for Efficient Inference on GPUs", section II-B (DW and PW convolutions) and
-section III-A (conv -> norm -> activation, up to six fused layers); "Fusing two back-to-back
+Convolutions for Efficient Inference on GPUs", section II-B (DW and PW convolutions),
+section II-D / Figure 3(b) (PWDW_R) and section III-A (conv -> norm -> activation, up to six
+fused layers); "Fusing two back-to-back
 convolutions" (CUTLASS discussion #208), the CONV1 3x3 -> CONV2 1x1 scale_bias_relu example.
 """
 from __future__ import annotations
@@ -55,10 +56,11 @@ def bind(path: str):
     lib.oracle_pw.argtypes = [i] * 5 + [dp] * 4 + [i, dp, i]
     lib.oracle_dense.argtypes = [i] * 8 + [dp] * 4 + [i, dp, i]
     lib.oracle_fused.argtypes = [i] * 10 + [dp] * 4 + [i] + [dp] * 3 + [i, i, dp, i]
+    lib.oracle_pwdw.argtypes = [i] * 8 + [dp] * 4 + [i] + [dp] * 3 + [i, i, dp, i]
     lib.oracle_round_format.argtypes = [ctypes.c_double, i, i, ctypes.c_double]
     lib.oracle_round_format.restype = ctypes.c_double
     lib.oracle_max_threads.argtypes = [i]
-    for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused,
+    for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused, lib.oracle_pwdw,
               lib.oracle_max_threads):
         f.restype = ctypes.c_int
     return lib
@@ -159,6 +161,26 @@ def fused(x, w1, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1, pad=0,
                               _ptr(b2), ACT[act2], MID[mid], _ptr(y), nthreads)
     if rc != 0:
         raise ValueError("oracle_fused: invalid shape")
+    return y
+
+
+def pwdw(x, wq, s1, b1, wd2, s2, b2, act1="none", act2="none", stride=1, pad=0, mid="exact",
+         nthreads=0, lib=None) -> np.ndarray:
+    """PWDW module in one pass: 1x1 conv wq [Cm,C] + scale/bias/act1, then depthwise
+    wd2 [Cm,k,k] over the intermediate (zero padding of the intermediate) + scale/bias/act2;
+    x [N,H,W,C] -> [N,Ho,Wo,Cm]."""
+    x, wq, s1, b1, wd2, s2, b2 = map(_f64, (x, wq, s1, b1, wd2, s2, b2))
+    N, H, W, C = x.shape
+    Cm, k = wd2.shape[0], wd2.shape[1]
+    assert wq.shape == (Cm, C) and wd2.shape == (Cm, k, k)
+    assert s1.shape == (Cm,) and b1.shape == (Cm,) and s2.shape == (Cm,) and b2.shape == (Cm,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    y = np.empty((N, Ho, Wo, Cm), np.float64)
+    rc = _load(lib).oracle_pwdw(N, H, W, C, Cm, k, stride, pad, _ptr(x), _ptr(wq), _ptr(s1),
+                                _ptr(b1), ACT[act1], _ptr(wd2), _ptr(s2), _ptr(b2), ACT[act2],
+                                MID[mid], _ptr(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pwdw: invalid shape")
     return y
 
 

@@ -16,6 +16,11 @@
  *  - Each convolution is followed by its normalization and activation layers; an FCM fuses
  *    up to six layers: two convolutions, each with its norm and activation (section III-A).
  *    With inference-time batch norm folded, norm is a per-channel scale and bias.
+ *  - PWDW case (an inverted residual's expansion and depthwise layers): a 1x1 convolution
+ *    followed by a depthwise k x k convolution of its output, each with its norm and
+ *    activation; the depthwise layer pads its own input, the intermediate, with zeros; the
+ *    values of the intermediate under overlapping tiles are recomputed by each tile (the
+ *    "_R" of PWDW_R, section II-D, Figure 3(b); sections III-A and IV-B).
  *  - Back-to-back case: a dense 3x3 convolution followed by a 1x1 convolution, each with a
  *    per-channel scale_bias_relu epilogue, NHWC activations ("Fusing two back-to-back
  *    convolutions", CUTLASS discussion #208, the CONV1/CONV2 example).
@@ -33,6 +38,8 @@
  *   wd [C][k][k]              depthwise filters
  *   w1 [K1][k][k][C]          dense conv1 filters (K, R, S, C)
  *   wp [K][Cm]                pointwise filters (Cm = C for DW, K1 for dense)
+ *   wq [Cm][C]                PWDW: pointwise filters of the first layer
+ *   wd2 [Cm][k][k]            PWDW: depthwise filters of the second layer
  *   m  [N][Ho][Wo][Cm]        intermediate feature maps
  *   y  [N][Ho][Wo][K]         output feature maps
  *
@@ -245,4 +252,43 @@ int oracle_fused(int dense, int N, int H, int W, int C, int Cm, int K, int k, in
         free(mid);
     }
     return failed ? -1 : 0;
+}
+
+/*
+ * The PWDW module as its own single pass: for every output pixel and channel j, the value of
+ * the intermediate under each depthwise tap is the 1x1 convolution of the input pixel there,
+ * recomputed on the spot, followed by its norm and activation (and the optional mirror
+ * rounding); taps that fall in the padding read zero, because the padding belongs to the
+ * depthwise layer's input.  It does not call oracle_pw/oracle_dw.
+ * x [N][H][W][C], wq [Cm][C], wd2 [Cm][k][k] -> y [N][Ho][Wo][Cm].
+ */
+int oracle_pwdw(int N, int H, int W, int C, int Cm, int k, int s, int p,
+                const double *x, const double *wq, const double *s1, const double *b1, int act1,
+                const double *wd2, const double *s2, const double *b2, int act2,
+                int mid_mode, double *y, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Cm < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int j = 0; j < Cm; j++) {
+                    double t = 0.0;
+                    for (int i = 0; i < k; i++) {
+                        int hi = ho * s - p + i;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int u = 0; u < k; u++) {
+                            int wi = wo * s - p + u;
+                            if (wi < 0 || wi >= W) continue;
+                            double q = 0.0;
+                            for (int c = 0; c < C; c++)
+                                q += x[IDX4(n, hi, wi, c, H, W, C)] * wq[(size_t)j * C + c];
+                            double mval = mid_round(act_apply(s1[j] * q + b1[j], act1), mid_mode);
+                            t += mval * wd2[((size_t)j * k + i) * k + u];
+                        }
+                    }
+                    y[IDX4(n, ho, wo, j, Ho, Wo, Cm)] = act_apply(s2[j] * t + b2[j], act2);
+                }
+    return 0;
 }

@@ -211,8 +211,66 @@ def pin_composition_integers(lib=None):
     return True
 
 
+def lib_pwdw(x, wq, s1, b1, wd2, s2, b2, a1, a2, stride, pad):
+    """1x1 conv (torch, float64) then grouped k x k conv with zero padding of the
+    intermediate."""
+    m = lib_pw(x, wq, s1, b1, a1)
+    return lib_dw(m, wd2, s2, b2, a2, stride, pad)
+
+
+PWDW_CASES = [  # N, H, W, C, Cm, k, s, p, act1, act2
+    (1, 1, 1, 1, 1, 3, 1, 1, "none", "none"), (1, 5, 5, 3, 4, 3, 1, 1, "relu6", "relu6"),
+    (2, 6, 5, 2, 3, 3, 2, 1, "relu", "none"), (1, 7, 6, 4, 2, 5, 1, 2, "none", "relu"),
+    (1, 6, 7, 3, 5, 3, 2, 0, "relu", "relu6"), (1, 3, 4, 2, 2, 1, 1, 0, "none", "none"),
+]
+
+
+def pin_pwdw(lib=None):
+    r = rng(41)
+    for (N, H, W, C, Cm, k, s, p, a1, a2) in PWDW_CASES:
+        x = r.uniform(-2, 2, (N, H, W, C))
+        wq = r.uniform(-1, 1, (Cm, C))
+        wd2 = r.uniform(-1, 1, (Cm, k, k))
+        s1, b1 = r.uniform(0.5, 1.5, Cm), r.uniform(-0.5, 0.5, Cm)
+        s2, b2 = r.uniform(0.5, 1.5, Cm), r.uniform(-0.5, 0.5, Cm)
+        got = oracle.pwdw(x, wq, s1, b1, wd2, s2, b2, a1, a2, s, p, lib=lib)
+        if not close(got, lib_pwdw(x, wq, s1, b1, wd2, s2, b2, a1, a2, s, p)):
+            return False
+    return True
+
+
+def pin_pwdw_padding_by_hand(lib=None):
+    """One pixel, one channel, 3x3 depthwise with pad 1: x = 2, 1x1 weight 3, scale 1, bias 5,
+    no activation -> the intermediate is 11; all taps 1, so only the centre tap is inside and
+    y = 2 * 11 + 1 = 23 (scale 2, bias 1).  Padding the input instead of the intermediate
+    would add act(0*3 + 5) = 5 for each of the 8 outer taps: 2 * 51 + 1 = 103."""
+    y = oracle.pwdw(np.full((1, 1, 1, 1), 2.0), [[3.0]], [1.0], [5.0], np.ones((1, 3, 3)), [2.0],
+                    [1.0], "none", "none", 1, 1, lib=lib)
+    return y.shape == (1, 1, 1, 1) and y[0, 0, 0, 0] == 23.0
+
+
+def pin_pwdw_composition_integers(lib=None):
+    """pwdw == dw(pw(x)) bit for bit on integer data (both oracle paths, stride 1 and 2)."""
+    r = rng(43)
+    C, Cm, k = 3, 4, 3
+    x = r.integers(-3, 4, (2, 6, 7, C)).astype(float)
+    wq = r.integers(-2, 3, (Cm, C)).astype(float)
+    wd2 = r.integers(-2, 3, (Cm, k, k)).astype(float)
+    b1 = r.integers(-2, 3, Cm).astype(float)
+    b2 = r.integers(-2, 3, Cm).astype(float)
+    one = np.ones(Cm)
+    for s in (1, 2):
+        m = oracle.pw(x, wq, one, b1, "relu6", lib=lib)
+        y = oracle.dw(m, wd2, one, b2, "relu", s, 1, lib=lib)
+        yf = oracle.pwdw(x, wq, one, b1, wd2, one, b2, "relu6", "relu", s, 1, lib=lib)
+        if not np.array_equal(y, yf):
+            return False
+    return True
+
+
 PINS = [pin_dw, pin_pw, pin_dense, pin_fused, pin_golden_dw, pin_golden_dense,
-        pin_delta_identity, pin_linearity, pin_composition_integers]
+        pin_delta_identity, pin_linearity, pin_composition_integers, pin_pwdw,
+        pin_pwdw_padding_by_hand, pin_pwdw_composition_integers]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -297,6 +355,15 @@ MUTANTS = {
                                "y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = act_apply(t + b2[kk], act2);"),
     "f16_round_precision": ("return oracle_round_format(v, 11, -14, 65504.0);",
                             "return oracle_round_format(v, 10, -14, 65504.0);"),
+    # taps left or right of the image read act1(s1*0 + b1), as if the input were padded
+    "pwdw_pads_the_input": ("                            if (wi < 0 || wi >= W) continue;\n                            double q = 0.0;",
+                            "                            if (wi < 0 || wi >= W) { t += act_apply(b1[j], act1) * wd2[((size_t)j * k + i) * k + u]; continue; }\n                            double q = 0.0;"),
+    "pwdw_pw_weight_transposed": ("q += x[IDX4(n, hi, wi, c, H, W, C)] * wq[(size_t)j * C + c];",
+                                  "q += x[IDX4(n, hi, wi, c, H, W, C)] * wq[(size_t)c * Cm + j];"),
+    "pwdw_pw_scale_dropped": ("double mval = mid_round(act_apply(s1[j] * q + b1[j], act1), mid_mode);",
+                              "double mval = mid_round(act_apply(q + b1[j], act1), mid_mode);"),
+    "pwdw_dw_tap_transposed": ("t += mval * wd2[((size_t)j * k + i) * k + u];",
+                               "t += mval * wd2[((size_t)j * k + u) * k + i];"),
 }
 
 
