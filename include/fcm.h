@@ -6,7 +6,14 @@
  *     m = act1(s1 * conv1(x) + b1)          conv1: depthwise k x k, or dense k x k
  *     y = act2(s2 * (m . wp^T) + b2)        1x1 pointwise convolution
  *
- * where the intermediate m never leaves the thread block (shared memory / tensor memory).
+ * or, for the PWDW module (FCM_CONV1_POINTWISE, an inverted residual's expansion and
+ * depthwise layers; the paper's PWDW_R, section II-D, Figure 3(b)):
+ *
+ *     m = act1(s1 * (x . w1^T) + b1)        1x1 pointwise convolution C -> Cm
+ *     y = act2(s2 * dw(m) + b2)             depthwise k x k over m (m zero-padded)
+ *
+ * where the intermediate m never leaves the thread block (shared memory / tensor memory);
+ * in the PWDW case every tile recomputes the intermediate under its depthwise halo.
  * Definitions: "Fusing Depthwise and Pointwise Convolutions for Efficient Inference on GPUs",
  * section II-B (DW and PW convolutions), section II-D (the DWPW tile must hold all channels),
  * section III (FCMs: up to six fused layers -- two convolutions, each followed by its
@@ -56,10 +63,19 @@ typedef enum fcm_status {
 
 typedef enum fcm_dtype { FCM_F32 = 0, FCM_F16 = 1, FCM_BF16 = 2 } fcm_dtype;
 typedef enum fcm_act { FCM_ACT_NONE = 0, FCM_ACT_RELU = 1, FCM_ACT_RELU6 = 2 } fcm_act;
-typedef enum fcm_conv1_kind { FCM_CONV1_DEPTHWISE = 0, FCM_CONV1_DENSE = 1 } fcm_conv1_kind;
+/* The module's layer pair.  DEPTHWISE and DENSE: a k x k first convolution, then 1x1.
+ * POINTWISE (PWDW): a 1x1 first convolution C -> Cm (Cm = mid, or C when mid is 0), then a
+ * depthwise k x k convolution over the Cm channels; k_out must equal Cm. */
+typedef enum fcm_conv1_kind {
+    FCM_CONV1_DEPTHWISE = 0,
+    FCM_CONV1_DENSE = 1,
+    FCM_CONV1_POINTWISE = 2
+} fcm_conv1_kind;
 
 /* What fcm_run computes.  The three non-fused modes are the layer-by-layer (LBL) baselines of
- * the paper's section V-C, built from the same building blocks as the fused kernels. */
+ * the paper's section V-C, built from the same building blocks as the fused kernels.  For
+ * FCM_CONV1_POINTWISE, "CONV1" is the 1x1 convolution (m is [N,H,W,Cm], the input's extent)
+ * and "PW_ONLY" runs the second convolution, the depthwise one, on m. */
 typedef enum fcm_mode {
     FCM_MODE_FUSED = 0,       /* in = x [N,H,W,C]    -> out = y [N,Ho,Wo,K]                 */
     FCM_MODE_CONV1_ONLY = 1,  /* in = x [N,H,W,C]    -> out = m [N,Ho,Wo,Cm] (storage dtype) */
@@ -75,8 +91,8 @@ typedef enum fcm_kernel_pref { FCM_KERNEL_AUTO = 0, FCM_KERNEL_SIMT = 1, FCM_KER
 typedef struct fcm_desc {
     int n, h, w, c;        /* input feature maps, NHWC                                     */
     int k_out;             /* 1x1 convolution output channels K                             */
-    int mid;               /* dense conv1 output channels Cm (0 = C); must be 0 or C for DW */
-    int ksize, stride, pad;/* conv1 filter size, stride, zero padding (square)              */
+    int mid;               /* first convolution's output channels Cm (0 = C); 0 or C for DW */
+    int ksize, stride, pad;/* the k x k convolution's filter size, stride, zero padding     */
     int conv1;             /* fcm_conv1_kind                                                */
     int dtype;             /* fcm_dtype of activations and weights                          */
     int act1, act2;        /* fcm_act after conv1 and after the 1x1 convolution             */
@@ -97,7 +113,8 @@ typedef struct fcm_plan_info {
     long long num_tiles;         /* output tiles over the whole batch                         */
     long long bytes_fused_min;   /* input + weights + scale/bias + output, each once          */
     long long bytes_unfused_min; /* the above + one write and one read of the intermediate    */
-    long long gma_fused_model;   /* DWPW estimator built from Eq. 1-3, bytes, whole batch     */
+    long long gma_fused_model;   /* DWPW estimator built from Eq. 1-3 (PWDW: Eq. 4), bytes,
+                                    whole batch                                               */
     long long gma_lbl_model;     /* Eq. 3 (DW) + Eq. 2 (PW), bytes, whole batch               */
     long long overlap_elems;     /* Eq. 1 for the chosen tile, elements per channel per image */
 } fcm_plan_info;
@@ -105,7 +122,8 @@ typedef struct fcm_plan_info {
 typedef struct fcm_handle fcm_handle;
 
 /* Create a module.  w1: DW filters [C][k][k] or dense filters [Cm][k][k][C]; wp: 1x1 filters
- * [K][Cm]; s1,b1: [Cm]; s2,b2: [K].  Each pointer may be host or device memory (unified
+ * [K][Cm]; s1,b1: [Cm]; s2,b2: [K].  PWDW (FCM_CONV1_POINTWISE): w1 is the 1x1 filters
+ * [Cm][C] and wp the depthwise filters [Cm][k][k]; s2,b2: [Cm].  Each pointer may be host or device memory (unified
  * addressing decides); the handle copies and repacks everything into device memory it owns,
  * so the caller may free its copies on return.  Rejects (FCM_ERR_UNSUPPORTED) a second
  * convolution that is not 1x1 by construction: there is no parameter for it.  Uses the

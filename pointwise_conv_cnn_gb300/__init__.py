@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "FCM_OK", 1: "FCM_ERR_INVALID_ARG", 2: "FCM_ERR_UNSUPPORTED",
                 6: "FCM_ERR_TIMEOUT", 7: "FCM_ERR_DEVICE_FAULT", 8: "FCM_ERR_NO_DEVICE"}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
-CONV1 = {"dw": 0, "dense": 1}
+CONV1 = {"dw": 0, "dense": 1, "pwdw": 2}
 MODES = {"fused": 0, "conv1": 1, "pw": 2, "unfused": 3}
 KERNELS = {"auto": 0, "simt": 1, "tc": 2}
 
@@ -161,7 +161,7 @@ def make_desc(n, h, w, c, k_out, ksize, stride, pad, conv1="dw", dtype="f16", ac
 def desc_from_workload(wl, **over) -> FcmDesc:
     kw = dict(n=wl.n, h=wl.h, w=wl.w, c=wl.c, k_out=wl.k_out, ksize=wl.ksize, stride=wl.stride,
               pad=wl.pad, conv1=wl.conv1, dtype=wl.dtype, act1=wl.act1, act2=wl.act2,
-              mid=wl.mid if wl.conv1 == "dense" else 0)
+              mid=wl.mid if wl.conv1 in ("dense", "pwdw") else 0)
     kw.update(over)
     return make_desc(**kw)
 

@@ -75,7 +75,8 @@ fcm_status fcm_tensor_bytes(const fcm_desc *desc, size_t *x_bytes, size_t *m_byt
     if (st != FCM_OK) return st;
     size_t e = desc->dtype == FCM_F32 ? 4 : 2;
     if (x_bytes) *x_bytes = (size_t)desc->n * desc->h * desc->w * desc->c * e;
-    if (m_bytes) *m_bytes = (size_t)desc->n * ho * wo * cm * e;
+    const bool pwdw = desc->conv1 == FCM_CONV1_POINTWISE;   // m keeps the input's extent
+    if (m_bytes) *m_bytes = (size_t)desc->n * (pwdw ? desc->h : ho) * (pwdw ? desc->w : wo) * cm * e;
     if (y_bytes) *y_bytes = (size_t)desc->n * ho * wo * desc->k_out * e;
     return FCM_OK;
 }
@@ -121,7 +122,8 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
     h->num_sms = prop.multiProcessorCount;
     h->smem_optin = (int)prop.sharedMemPerBlockOptin;
     h->x_elems = (size_t)desc->n * desc->h * desc->w * desc->c;
-    h->m_elems = (size_t)desc->n * ho * wo * cm;
+    const bool pwdw = desc->conv1 == FCM_CONV1_POINTWISE;
+    h->m_elems = pwdw ? (size_t)desc->n * desc->h * desc->w * cm : (size_t)desc->n * ho * wo * cm;
     h->y_elems = (size_t)desc->n * ho * wo * desc->k_out;
 
     st = fcm_make_plan(desc, h->num_sms, h->smem_optin, &h->plan, &h->tc);
@@ -132,8 +134,8 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
 
     const int C = desc->c, K = desc->k_out, k = desc->ksize, dt = desc->dtype;
     const bool dense = desc->conv1 == FCM_CONV1_DENSE;
-    const size_t n_w1 = dense ? (size_t)cm * k * k * C : (size_t)C * k * k;
-    const size_t n_wp = (size_t)K * cm;
+    const size_t n_w1 = dense ? (size_t)cm * k * k * C : pwdw ? (size_t)cm * C : (size_t)C * k * k;
+    const size_t n_wp = pwdw ? (size_t)cm * k * k : (size_t)K * cm;
     std::vector<unsigned char> hw1, hwp, hs1, hb1, hs2, hb2;
     if ((st = fetch(hw1, w1, n_w1 * h->esize, "w1")) != FCM_OK ||
         (st = fetch(hwp, wp, n_wp * h->esize, "wp")) != FCM_OK ||
@@ -145,9 +147,17 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
         return st;
     }
 
-    // SIMT layouts: conv1 taps major ([k*k][C] for DW, [k*k*C][Cm] for dense), wp as [Cm][K]
+    // SIMT layouts: conv1 taps major ([k*k][C] for DW, [k*k*C][Cm] for dense), wp as [Cm][K];
+    // PWDW: the 1x1 filters as [C][Cm] (the 1x1 kernel's layout), the depthwise taps [k*k][Cm]
     std::vector<float> w1t(n_w1), wpt(n_wp);
-    if (dense) {
+    if (pwdw) {
+        for (int j = 0; j < cm; j++)
+            for (int c = 0; c < C; c++)
+                w1t[(size_t)c * cm + j] = host_to_f(hw1.data(), (size_t)j * C + c, dt);
+        for (int j = 0; j < cm; j++)
+            for (int t = 0; t < k * k; t++)
+                wpt[(size_t)t * cm + j] = host_to_f(hwp.data(), (size_t)j * k * k + t, dt);
+    } else if (dense) {
         for (int j = 0; j < cm; j++)
             for (int t = 0; t < k * k; t++)
                 for (int c = 0; c < C; c++)
@@ -157,8 +167,10 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
             for (int t = 0; t < k * k; t++)
                 w1t[(size_t)t * C + c] = host_to_f(hw1.data(), (size_t)c * k * k + t, dt);
     }
-    for (int kk = 0; kk < K; kk++)
-        for (int c = 0; c < cm; c++) wpt[(size_t)c * K + kk] = host_to_f(hwp.data(), (size_t)kk * cm + c, dt);
+    if (!pwdw)
+        for (int kk = 0; kk < K; kk++)
+            for (int c = 0; c < cm; c++)
+                wpt[(size_t)c * K + kk] = host_to_f(hwp.data(), (size_t)kk * cm + c, dt);
 
     if ((st = upload(&h->w1t, w1t.data(), w1t.size())) != FCM_OK ||
         (st = upload(&h->wpt, wpt.data(), wpt.size())) != FCM_OK ||
@@ -204,6 +216,22 @@ static fcm_status run_one(fcm_handle *h, int mode, const void *in, void *out, cu
     const bool tc = h->plan.kernel == FCM_KERNEL_TC;
     const bool dense = h->d.conv1 == FCM_CONV1_DENSE;
     cudaError_t e = cudaSuccess;
+    if (h->d.conv1 == FCM_CONV1_POINTWISE) {
+        switch (mode) {
+        case FCM_MODE_FUSED:
+            e = tc ? launch_tc_pwdw(h, in, out, st) : launch_pwdw_fused_simt(h, in, out, st);
+            break;
+        case FCM_MODE_CONV1_ONLY:
+            e = tc ? launch_tc_pwdw_first(h, in, out, st) : launch_pwdw_first_simt(h, in, out, st);
+            break;
+        case FCM_MODE_PW_ONLY:
+            e = tc ? launch_tc_pwdw_second(h, in, out, st) : launch_pwdw_second_simt(h, in, out, st);
+            break;
+        default: return fcm_fail(FCM_ERR_INVALID_ARG, "mode %d", mode);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        return FCM_OK;
+    }
     switch (mode) {
     case FCM_MODE_FUSED:
         e = tc ? (dense ? launch_tc_b2b(h, mode, in, out, st) : launch_tc_dwpw(h, mode, in, out, st))

@@ -35,6 +35,7 @@ struct fcm_handle {
     fcm_desc d{};
     fcm_plan_info plan{};
     TcPlan tc{};
+    TcPlan tc2{};             // PWDW: plan of the layer-by-layer depthwise stage
     int device = -1;
     int ho = 0, wo = 0, cm = 0;
     int esize = 0;
@@ -76,7 +77,19 @@ fcm_status fcm_b2b_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, 
                         TcPlan *tc);
 fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_host);
 
+// tc_pwdw.cu: 1x1 -> depthwise (PWDW) on tcgen05 + CUDA cores
+int fcm_pwdw_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);
+fcm_status fcm_pwdw_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
+                         TcPlan *tc);
+fcm_status fcm_pwdw_prepare(fcm_handle *h, const void *w1_host, const void *wp_host);
+cudaError_t launch_tc_pwdw(const fcm_handle *h, const void *x, void *y, cudaStream_t st);
+cudaError_t launch_tc_pwdw_first(const fcm_handle *h, const void *x, void *m, cudaStream_t st);
+cudaError_t launch_tc_pwdw_second(const fcm_handle *h, const void *m, void *y, cudaStream_t st);
+
 // simt_kernels.cu
+cudaError_t launch_pwdw_fused_simt(const fcm_handle *h, const void *x, void *y, cudaStream_t st);
+cudaError_t launch_pwdw_first_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st);
+cudaError_t launch_pwdw_second_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st);
 cudaError_t launch_conv1_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st);
 cudaError_t launch_pw_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st);
 cudaError_t launch_fused_simt(const fcm_handle *h, const void *x, void *y, cudaStream_t st);

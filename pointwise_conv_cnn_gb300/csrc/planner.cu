@@ -64,7 +64,8 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
         return fcm_fail(FCM_ERR_UNSUPPORTED, "stride %d outside 1..2", d->stride);
     if (d->pad < 0 || d->pad >= d->ksize)
         return fcm_fail(FCM_ERR_INVALID_ARG, "pad %d must be in [0, ksize)", d->pad);
-    if (d->conv1 != FCM_CONV1_DEPTHWISE && d->conv1 != FCM_CONV1_DENSE)
+    if (d->conv1 != FCM_CONV1_DEPTHWISE && d->conv1 != FCM_CONV1_DENSE &&
+        d->conv1 != FCM_CONV1_POINTWISE)
         return fcm_fail(FCM_ERR_INVALID_ARG, "conv1 kind %d", d->conv1);
     if (d->dtype < FCM_F32 || d->dtype > FCM_BF16)
         return fcm_fail(FCM_ERR_INVALID_ARG, "dtype %d", d->dtype);
@@ -80,6 +81,10 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
         return fcm_fail(FCM_ERR_INVALID_ARG, "depthwise conv1 keeps the channel count (mid %d != c %d)",
                         d->mid, d->c);
     if (m < 1) return fcm_fail(FCM_ERR_INVALID_ARG, "mid channels %d", m);
+    if (d->conv1 == FCM_CONV1_POINTWISE && d->k_out != m)
+        return fcm_fail(FCM_ERR_INVALID_ARG,
+                        "PWDW: the depthwise layer keeps the channel count (k_out %d != mid %d)",
+                        d->k_out, m);
     int h_o = out_extent(d->h, d->ksize, d->stride, d->pad);
     int w_o = out_extent(d->w, d->ksize, d->stride, d->pad);
     if (h_o < 1 || w_o < 1) return fcm_fail(FCM_ERR_INVALID_ARG, "empty output");
@@ -105,15 +110,31 @@ static void fill_bytes(const fcm_desc *d, int ho, int wo, int cm, int th, int tw
                        fcm_plan_info *info) {
     long long e = d->dtype == FCM_F32 ? 4 : 2;
     long long N = d->n, H = d->h, W = d->w, C = d->c, K = d->k_out, k = d->ksize;
-    long long x = N * H * W * C, mid = N * ho * wo * cm, y = N * ho * wo * K;
-    long long w1 = d->conv1 == FCM_CONV1_DENSE ? (long long)cm * k * k * C : C * k * k;
-    long long wp = K * cm;
+    const bool pwdw = d->conv1 == FCM_CONV1_POINTWISE;
+    long long x = N * H * W * C, y = N * ho * wo * K;
+    long long mid = pwdw ? N * H * W * cm : N * ho * wo * cm;
+    long long w1 = d->conv1 == FCM_CONV1_DENSE ? (long long)cm * k * k * C
+                   : pwdw                      ? (long long)cm * C
+                                               : C * k * k;
+    long long wp = pwdw ? (long long)cm * k * k : K * cm;
     long long sb = 4 * (2LL * cm + 2LL * K);
     info->bytes_fused_min = (x + y + w1 + wp) * e + sb;
     info->bytes_unfused_min = info->bytes_fused_min + 2 * mid * e;
     long long s = d->stride;
     long long ov = fcm_model_overlap(W, H, (long long)tw * s, (long long)th * s, k, k, s);
     info->overlap_elems = ov;
+    if (pwdw) {
+        // PW (C -> Cm over H x W) then DW (Cm, k x k): Eq. 2 + Eq. 3 layer by layer, Eq. 4 fused
+        // (the tile holds all Cm channels: weight tiles are whole)
+        long long hw = H * W, ohw = (long long)ho * wo, thw = (long long)th * tw;
+        long long lbl_pw = fcm_model_pw_gma(w1, w1, hw * C, hw * cm, thw * cm);
+        long long lbl_dw = fcm_model_dw_gma(cm, ov, hw * cm, ohw * cm, ohw, thw, wp);
+        long long fused = fcm_model_pwdw_gma(C, ov, hw * C, w1, w1, wp, wp, ohw * cm, thw * cm,
+                                             ohw, thw);
+        info->gma_lbl_model = (lbl_pw + lbl_dw) * N * e;
+        info->gma_fused_model = fused * N * e;
+        return;
+    }
     long long ifm = H * W * C, ofm1 = (long long)ho * wo * cm, ofm = (long long)ho * wo * K;
     long long lbl_dw = fcm_model_dw_gma(C, ov, ifm, ofm1, (long long)ho * wo, (long long)th * tw, w1);
     long long lbl_pw = fcm_model_pw_gma(wp, wp, ofm1, ofm, (long long)th * tw * K);
@@ -160,7 +181,7 @@ fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm
         // SIMT kernels: flattened tiles of 32 output pixels, all channels
         const int px = 32;
         long long P = (long long)d->n * ho * wo;
-        long long smem = 4LL * px * cm;
+        long long smem = d->conv1 == FCM_CONV1_POINTWISE ? 0 : 4LL * px * cm;
         if (smem > smem_per_block)
             return fcm_fail(FCM_ERR_SMEM_BUDGET, "commBuffer of %lld bytes exceeds %d", smem,
                             smem_per_block);

@@ -196,6 +196,45 @@ __global__ void __launch_bounds__(kThreads) k_fused(
     }
 }
 
+// PWDW in one pass: thread item = (output pixel, channel j).  The intermediate under each
+// depthwise tap is the 1x1 convolution of the input pixel there, recomputed (PWDW_R), rounded
+// to the storage type as the layer-by-layer path stores it; taps over the padding read zero.
+// Same operation order as k_pw followed by k_conv1_dw, so fused == unfused bit for bit.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_fused_pwdw(
+    const T *__restrict__ x, const float *__restrict__ wq, const float *__restrict__ s1,
+    const float *__restrict__ b1, const float *__restrict__ wd, const float *__restrict__ s2,
+    const float *__restrict__ b2, T *__restrict__ y, int N, int H, int W, int C, int Cm, int Ho,
+    int Wo, int k, int s, int p, int act1, int act2) {
+    const long long total = (long long)N * Ho * Wo * Cm;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(idx % Cm);
+        const long long pix = idx / Cm;
+        const int wo = (int)(pix % Wo);
+        const long long t = pix / Wo;
+        const int ho = (int)(t % Ho);
+        const int n = (int)(t / Ho);
+        float acc = 0.0f;
+        for (int i = 0; i < k; i++) {
+            const int hi = ho * s - p + i;
+            if (hi < 0 || hi >= H) continue;
+            for (int u = 0; u < k; u++) {
+                const int wi = wo * s - p + u;
+                if (wi < 0 || wi >= W) continue;
+                const T *xp = x + (((size_t)n * H + hi) * W + wi) * C;
+                float q = 0.0f;
+                for (int c = 0; c < C; c++)
+                    q = fmaf(Storage<T>::to_f(xp[c]), __ldg(wq + (size_t)c * Cm + j), q);
+                const float mval = Storage<T>::to_f(Storage<T>::from_f(
+                    act_apply(fmaf(__ldg(s1 + j), q, __ldg(b1 + j)), act1)));
+                acc = fmaf(mval, __ldg(wd + (size_t)(i * k + u) * Cm + j), acc);
+            }
+        }
+        y[idx] = Storage<T>::from_f(act_apply(fmaf(__ldg(s2 + j), acc, __ldg(b2 + j)), act2));
+    }
+}
+
 int grid_for(long long work_items, int threads, int num_sms) {
     long long blocks = (work_items + threads - 1) / threads;
     long long cap = (long long)num_sms * 8;
@@ -274,8 +313,75 @@ cudaError_t fused_t(const fcm_handle *h, const void *xin, void *yout, cudaStream
     return cudaGetLastError();
 }
 
+// PWDW layer by layer: the 1x1 convolution x -> m [N,H,W,Cm] (k_pw with C inputs), then the
+// depthwise convolution m -> y (k_conv1_dw over Cm channels).
+template <typename T>
+cudaError_t pwdw_first_t(const fcm_handle *h, const void *xin, void *mout, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    long long P = (long long)d.n * d.h * d.w;
+    size_t smem = sizeof(float) * kPwPixels * d.c;
+    cudaError_t e = cudaFuncSetAttribute(k_pw<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    long long blocks = (P + kPwPixels - 1) / kPwPixels;
+    int grid = (int)(blocks < (long long)h->num_sms * 8 ? blocks : (long long)h->num_sms * 8);
+    k_pw<T><<<grid, kThreads, smem, st>>>(static_cast<const T *>(xin), h->w1t, h->s1, h->b1,
+                                          static_cast<T *>(mout), P, d.c, h->cm, d.act1);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t pwdw_second_t(const fcm_handle *h, const void *min, void *yout, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    const T *m = static_cast<const T *>(min);
+    T *y = static_cast<T *>(yout);
+    constexpr int V16 = 16 / (int)sizeof(T);
+    if (h->cm % V16 == 0) {
+        long long items = (long long)d.n * h->ho * h->wo * (h->cm / V16);
+        k_conv1_dw<T, V16><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+            m, h->wpt, h->s2, h->b2, y, d.n, d.h, d.w, h->cm, h->ho, h->wo, d.ksize, d.stride,
+            d.pad, d.act2);
+    } else {
+        long long items = (long long)d.n * h->ho * h->wo * h->cm;
+        k_conv1_dw<T, 1><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+            m, h->wpt, h->s2, h->b2, y, d.n, d.h, d.w, h->cm, h->ho, h->wo, d.ksize, d.stride,
+            d.pad, d.act2);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t pwdw_fused_t(const fcm_handle *h, const void *xin, void *yout, cudaStream_t st) {
+    const fcm_desc &d = h->d;
+    long long items = (long long)d.n * h->ho * h->wo * h->cm;
+    k_fused_pwdw<T><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
+        static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
+        static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, h->ho, h->wo, d.ksize, d.stride,
+        d.pad, d.act1, d.act2);
+    return cudaGetLastError();
+}
+
 }  // namespace
 }  // namespace fcm
+
+#define FCM_BY_DTYPE(fn, ...)                                              \
+    switch (h->d.dtype) {                                                   \
+    case FCM_F32: return fcm::fn<float>(__VA_ARGS__);                       \
+    case FCM_F16: return fcm::fn<__half>(__VA_ARGS__);                      \
+    default: return fcm::fn<__nv_bfloat16>(__VA_ARGS__);                   \
+    }
+
+cudaError_t launch_pwdw_fused_simt(const fcm_handle *h, const void *x, void *y, cudaStream_t st) {
+    FCM_BY_DTYPE(pwdw_fused_t, h, x, y, st)
+}
+
+cudaError_t launch_pwdw_first_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st) {
+    FCM_BY_DTYPE(pwdw_first_t, h, x, m, st)
+}
+
+cudaError_t launch_pwdw_second_simt(const fcm_handle *h, const void *m, void *y, cudaStream_t st) {
+    FCM_BY_DTYPE(pwdw_second_t, h, m, y, st)
+}
 
 cudaError_t launch_conv1_simt(const fcm_handle *h, const void *x, void *m, cudaStream_t st) {
     switch (h->d.dtype) {

@@ -251,10 +251,11 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
         const int nw = a.C * KS * KS / 8;
         for (int i = threadIdx.x; i < nw; i += blockDim.x) wdw_s[i] = a.wdw[i];
     }
-    for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
-        s1_s[i] = a.s1[i];
-        b1_s[i] = a.b1[i];
-    }
+    if (has_dw)
+        for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
+            s1_s[i] = a.s1[i];
+            b1_s[i] = a.b1[i];
+        }
     for (int i = threadIdx.x; i < a.K; i += blockDim.x) {
         s2_s[i] = a.s2[i];
         b2_s[i] = a.b2[i];
@@ -668,6 +669,7 @@ int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why
         return 0;
     };
     if (d->dtype == FCM_F32) return no("fp32 runs on CUDA cores");
+    if (d->conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_supported(d, ho, wo, cm, why);
     if (d->conv1 != FCM_CONV1_DEPTHWISE) return fcm_b2b_supported(d, ho, wo, cm, why);
     if (cm % 16 != 0) return no("channels must be a multiple of 16");
     if (d->k_out % 16 != 0 || d->k_out < 16 || d->k_out > 256)
@@ -682,6 +684,7 @@ int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why
 fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_cap,
                        TcPlan *p) {
     if (d->conv1 == FCM_CONV1_DENSE) return fcm_b2b_plan(d, ho, wo, cm, num_sms, smem_cap, p);
+    if (d->conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_plan(d, ho, wo, cm, num_sms, smem_cap, p);
     const int S = d->stride, KS = d->ksize, C = cm;
     TcPlan best;
     double best_score = -1.0;
@@ -767,6 +770,7 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
 
 fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_host) {
     if (h->d.conv1 == FCM_CONV1_DENSE) return fcm_b2b_prepare(h, w1_host, wp_host);
+    if (h->d.conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_prepare(h, w1_host, wp_host);
     const fcm_desc &d = h->d;
     const int C = h->cm, K = d.k_out, KS = d.ksize, nkb = (C + 63) / 64;
     // B operand image: row n = output channel, K-dim = input channel, 128B swizzle

@@ -115,7 +115,9 @@ def numpy_storage_dtype(dtype: str):
 @dataclass(frozen=True)
 class Workload:
     """One fused layer pair.  conv1 is "dw" (weights [C,k,k]) or "dense" (weights
-    [Cm,k,k,C]); the 1x1 conv has weights [K,Cm]; activations are NHWC."""
+    [Cm,k,k,C]) followed by the 1x1 conv with weights [K,Cm]; or "pwdw": a 1x1 conv with
+    weights [Cm,C] followed by a depthwise k x k conv with weights [Cm,k,k] (K = Cm).
+    Activations are NHWC."""
     name: str
     n: int
     h: int
@@ -130,7 +132,7 @@ class Workload:
     act2: str
     dtype: str
     dist: str
-    mid: int = 0          # dense conv1 output channels (0: equal to c)
+    mid: int = 0          # first convolution's output channels (0: equal to c)
 
     @property
     def cm(self) -> int:
@@ -153,6 +155,10 @@ class Workload:
 
     def shapes(self) -> dict:
         k, C, Cm, K = self.ksize, self.c, self.cm, self.k_out
+        if self.conv1 == "pwdw":
+            return {"x": (self.n, self.h, self.w, C), "w1": (Cm, C), "wp": (Cm, k, k),
+                    "s1": (Cm,), "b1": (Cm,), "s2": (Cm,), "b2": (Cm,),
+                    "y": (self.n, self.ho, self.wo, Cm), "m": (self.n, self.h, self.w, Cm)}
         w1 = (C, k, k) if self.conv1 == "dw" else (Cm, k, k, C)
         return {"x": (self.n, self.h, self.w, C), "w1": w1, "wp": (K, Cm),
                 "s1": (Cm,), "b1": (Cm,), "s2": (K,), "b2": (K,),
@@ -160,6 +166,8 @@ class Workload:
 
     def fan_in(self) -> tuple[int, int]:
         k = self.ksize
+        if self.conv1 == "pwdw":
+            return self.c, k * k
         return (k * k if self.conv1 == "dw" else k * k * self.c), self.cm
 
     def min_bytes(self) -> dict:
@@ -178,6 +186,10 @@ class Workload:
     def flops(self) -> dict:
         P = self.n * self.ho * self.wo
         k = self.ksize
+        if self.conv1 == "pwdw":   # algorithmic: the 1x1 over H x W, the depthwise over Ho x Wo
+            pw = 2 * self.c * self.cm * self.n * self.h * self.w
+            dw = 2 * k * k * self.cm * P
+            return {"conv1": pw, "pw": dw, "total": pw + dw}
         conv1 = 2 * k * k * (self.c if self.conv1 == "dw" else self.c * self.cm) * P
         if self.conv1 == "dw":
             conv1 = 2 * k * k * self.c * P
@@ -198,6 +210,10 @@ WORKLOADS = (
     # two 1x1 convolutions back to back (the PWPW pair): 64 -> 128 (ReLU6) -> 64 (linear)
     Workload("pwpw_f16", 64, 56, 56, 64, 64, "dense", 1, 1, 0, "relu6", "none", "f16", "normal",
              mid=128),
+    # an inverted residual's expansion and depthwise layers (the PWDW pair): 1x1 64 -> 192
+    # (ReLU6), then depthwise 3x3 s1 over the 192 channels (ReLU6)
+    Workload("pwdw_f16", 64, 56, 56, 64, 192, "pwdw", 3, 1, 1, "relu6", "relu6", "f16", "normal",
+             mid=192),
 )
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -273,6 +289,12 @@ def integer_safe(wl: Workload, kind: str = "integer") -> bool:
     representable in the storage format (2^8 for bf16, 2^11 for f16)."""
     k = wl.ksize
     prod = 6 if kind == "integer" else 1
+    if wl.conv1 == "pwdw":
+        # the 1x1 sum over C, then k*k depthwise products of the intermediate
+        per1 = wl.c * prod + 2
+        lim = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8}[wl.dtype]
+        mid_max = min(per1, 6) if wl.act1 == "relu6" else per1
+        return per1 <= lim and k * k * mid_max * (prod // 3 + 1) + 2 < (1 << 24)
     per1 = k * k * (wl.c if wl.conv1 == "dense" else 1) * prod + 2
     lim = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8}[wl.dtype]
     mid_max = min(per1, 6) if wl.act1 == "relu6" else per1

@@ -68,6 +68,9 @@ def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
 def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.ndarray:
     f = case.f64()
     wl = case.wl
+    if wl.conv1 == "pwdw":
+        return oracle.pwdw(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
+                           wl.act1, wl.act2, wl.stride, wl.pad, mid=mid, nthreads=nthreads)
     return oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"], wl.act1,
                         wl.act2, wl.stride, wl.pad, conv1=wl.conv1, mid=mid, nthreads=nthreads)
 
@@ -75,14 +78,20 @@ def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.nda
 def oracle_conv1(case: wk.Case) -> np.ndarray:
     f = case.f64()
     wl = case.wl
+    if wl.conv1 == "pwdw":   # the 1x1 layer, over the input's extent
+        return oracle.pw(f["x"], f["w1"], f["s1"], f["b1"], wl.act1)
     if wl.conv1 == "dw":
         return oracle.dw(f["x"], f["w1"], f["s1"], f["b1"], wl.act1, wl.stride, wl.pad)
     return oracle.dense(f["x"], f["w1"], f["s1"], f["b1"], wl.act1, wl.stride, wl.pad)
 
 
 def oracle_pw(case: wk.Case, m: np.ndarray) -> np.ndarray:
+    """The module's second convolution on an intermediate (the depthwise one for PWDW)."""
     f = case.f64()
-    return oracle.pw(m, f["wp"], f["s2"], f["b2"], case.wl.act2)
+    wl = case.wl
+    if wl.conv1 == "pwdw":
+        return oracle.dw(m, f["wp"], f["s2"], f["b2"], wl.act2, wl.stride, wl.pad)
+    return oracle.pw(m, f["wp"], f["s2"], f["b2"], wl.act2)
 
 
 def parity_error(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str) -> float:

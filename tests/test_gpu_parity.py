@@ -147,6 +147,41 @@ def test_dense_edge_shapes(cuda, shape, kernel):
         assert_bitexact(got, oracle_fused(icase), dt)
 
 
+PWDW_EDGE = [  # (N, H, W, C, Cm, k, s, p, dtype, act1, act2): 1x1 C -> Cm, then depthwise k x k
+    (2, 9, 13, 64, 64, 3, 1, 1, "f16", "relu6", "relu6"),
+    (1, 11, 60, 64, 128, 3, 2, 1, "bf16", "relu", "none"),
+    (3, 7, 20, 128, 64, 5, 1, 2, "f16", "none", "relu"),
+    (1, 5, 100, 64, 64, 3, 1, 1, "f16", "relu", "relu"),
+    (2, 6, 6, 64, 192, 1, 1, 0, "bf16", "relu", "relu"),
+    (1, 13, 17, 32, 48, 3, 1, 1, "f16", "relu6", "none"),
+    (1, 9, 9, 8, 16, 3, 2, 1, "f32", "relu", "relu6"),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("shape", PWDW_EDGE, ids=lambda s: "x".join(map(str, s[:8])) + s[8])
+def test_pwdw_edge_shapes(cuda, shape, kernel):
+    """PWDW: tiles whose halo crosses the image border (the intermediate is zero there, not
+    act(bias)), stride 2, 5x5, several M blocks per halo, k = 1."""
+    N, H, W, C, mid, k, s, p, dt, a1, a2 = shape
+    wl = wk.Workload("pwdw_edge", N, H, W, C, mid, "pwdw", k, s, p, a1, a2, dt, "normal", mid=mid)
+    case = wk.make_case(wl, seed=7)
+    mod = module_or_skip(case, kernel)
+    ref = oracle_fused(case)
+    got, _ = run_case(case, "fused", module=mod)
+    assert_parity(got, ref, dt, max(C, k * k))   # longest reduction on the path (fp32 bar)
+    got_u, _ = run_case(case, "unfused", module=mod)
+    assert_parity(got_u, ref, dt, max(C, k * k))
+    kind = "integer" if wk.integer_safe(wl) else "integer1"
+    if wk.integer_safe(wl, kind):
+        icase = wk.make_case(wl, seed=8, kind=kind)
+        imod = make_module(icase, kernel) if kernel != "tc" else module_or_skip(icase, kernel)
+        iref = oracle_fused(icase)
+        for mode in ("fused", "unfused"):
+            got, _ = run_case(icase, mode, module=imod)
+            assert_bitexact(got, iref, dt)
+
+
 def test_run_host_matches_run(cuda):
     import torch
     wl = reduced(wk.BY_NAME["mobilenet_dwpw_f16"], n=2)
