@@ -13,7 +13,7 @@
 //              operand, one row per halo pixel, in M blocks of 128 rows
 //   MMA        1x1 convolution for one 64-channel chunk of the intermediate:
 //              D[halo pixel, 64] = A x W1[chunk]^T into TMEM (double-buffered)
-//   mid        4 warps: TMEM -> scale/bias/act1 -> 16-bit -> the commBuffer in shared memory
+//   mid        8 warps: TMEM -> scale/bias/act1 -> 16-bit -> the commBuffer in shared memory
 //              (one 128-byte row per halo pixel, 16-byte chunks swizzled by the pixel index);
 //              halo pixels outside the image are written as zeros -- the depthwise layer pads
 //              its own input, the intermediate
@@ -37,10 +37,10 @@ namespace pwdw {
 
 using namespace fcm::tc;
 
-constexpr int kMidWarps = 4;
+constexpr int kMidWarps = 8;     // two per TMEM lane quadrant: even and odd M blocks
 constexpr int kFirstDwWarp = 2 + kMidWarps;
 constexpr int kMaxDwWarps = 10;
-constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);   // 16 warps: 128 registers
+constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);
 constexpr int kR = 4;           // output pixels per DW work unit (along W)
 constexpr int kCt = 64;         // intermediate channels per work item
 constexpr int kMaxBlk = 4;      // M blocks of 128 halo pixels
@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
         __syncwarp();
     } else if (warp < kFirstDwWarp) {
         // ===================================================== mid epilogue
-        const int q = warp & 3;
+        const int q = warp & 3;          // TMEM lane quadrant
+        const int half = (warp - 2) >> 2; // this warp converts the M blocks of this parity
         const int RQ = a.R * a.Q;
         with_act(a.act1, [&](auto act_tag) {
             constexpr int ACT = decltype(act_tag)::value;
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
                     }
                     tc_fence_after();
                     const uint32_t comm_s = base_s + a.off_comm + (uint32_t)b * a.comm_bytes;
-                    for (int blk = 0; blk < a.nblk; blk++) {
+                    for (int blk = half; blk < a.nblk; blk += 2) {
                         const int pix = blk * 128 + q * 32 + lane;
                         const int r = pix / a.Q, c = pix - (pix / a.Q) * a.Q;
                         const int ih = ho0 * S - a.pad + r, iw = c - a.pad;
@@ -331,13 +332,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
                                     const int cg = j * kCt + cc;
                                     uint32_t pk[8];
 #pragma unroll
-                                    for (int i2 = 0; i2 < 8; i2++) {
-                                        const float v0 = fmaf(s1_s[cg + 2 * i2], __uint_as_float(rr[2 * i2]),
-                                                              b1_s[cg + 2 * i2]);
-                                        const float v1 = fmaf(s1_s[cg + 2 * i2 + 1],
-                                                              __uint_as_float(rr[2 * i2 + 1]),
-                                                              b1_s[cg + 2 * i2 + 1]);
-                                        pk[i2] = inside ? Pack2<T>::template run<ACT>(v0, v1) : 0u;
+                                    for (int i4 = 0; i4 < 4; i4++) {
+                                        const float4 sc = *reinterpret_cast<const float4 *>(s1_s + cg + 4 * i4);
+                                        const float4 bi = *reinterpret_cast<const float4 *>(b1_s + cg + 4 * i4);
+                                        const float v0 = fmaf(sc.x, __uint_as_float(rr[4 * i4]), bi.x);
+                                        const float v1 = fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y);
+                                        const float v2 = fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z);
+                                        const float v3 = fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w);
+                                        pk[2 * i4] = inside ? Pack2<T>::template run<ACT>(v0, v1) : 0u;
+                                        pk[2 * i4 + 1] = inside ? Pack2<T>::template run<ACT>(v2, v3) : 0u;
                                     }
                                     const uint32_t ch = (uint32_t)(cc >> 3);
                                     sts128(row_s + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
