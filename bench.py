@@ -252,6 +252,27 @@ def cpu_baseline(wk, wl, seconds: float) -> dict:
                       f"oracle_fused, {threads} OpenMP threads, {t:.2f} s"}
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time), or `value` alone when
+    there is no process group.  `device` is where the reduction tensor lives (cuda for NCCL,
+    cpu for gloo)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank: int, images_per_rank: int, world: int, region_ms: float,
+                   steps: int) -> tuple[float, float]:
+    """Whole-job GB/s and images/s: every rank runs its own replica of the step (weak
+    scaling), so the job moves world x the per-rank bytes in the slowest rank's time."""
+    step_s = region_ms / 1e3 / steps
+    return bytes_per_rank * world / step_s / 1e9, images_per_rank * world / step_s
+
+
 def run_ours(args):
     import torch
     import pointwise_conv_cnn_gb300 as fcm
@@ -275,17 +296,10 @@ def run_ours(args):
     wl = wk.BY_NAME[args.workload]
     res = time_ours(torch, fcm, wk, wl, args.mode, args.kernel, args.steps, args.warmup, device,
                     dist, sample_clocks=(local == 0))
-    region_ms = res["region_ms"]
-    if dist is not None:
-        t = torch.tensor([region_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(res["region_ms"], dist, device)
     steps = args.steps
     mb = wl.min_bytes()
-    step_s = region_ms / 1e3 / steps
-    bytes_per_step = mb["fused"] * world
-    value = bytes_per_step / step_s / 1e9
-    images_per_s = wl.n * world / step_s
+    value, images_per_s = job_throughput(mb["fused"], wl.n, world, region_ms, steps)
     peaks = load_peaks()
     kern_s = res["kernel_ms_mean"] / 1e3
     achieved = mb["fused"] / kern_s / 1e9
