@@ -15,8 +15,8 @@
 //   mid    TMEM -> registers -> scale/bias/act -> 16-bit -> the A operand of conv2 in shared
 //          memory (128-byte swizzled, K-major): the intermediate never leaves the SM.
 //   conv2  1x1 GEMM into a second TMEM accumulator.
-//   out    TMEM -> scale/bias/act -> 16-bit -> swizzled staging -> TMA tensor stores, one per
-//          output row and 64-channel block, clipped at Wo.
+//   out    TMEM -> scale/bias/act -> 16-bit -> swizzled staging (two tiles) -> TMA tensor
+//          stores, one per output row and 64-channel block, clipped at Wo.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5 mid epilogue,
 // warps 6-9 output epilogue.  Accumulators are double-buffered so conv1 of tile t overlaps
@@ -61,6 +61,7 @@ struct Args {
     uint32_t tmem_cols, idesc1, idesc2;
     uint32_t w1_bytes, w2_bytes, plane_bytes, in_stage_bytes, in_stage_stride;
     uint32_t off_w1, off_w2, off_a2, off_out, off_in, off_sb, off_bar;
+    uint32_t out_bytes;     // one output staging tile (FUSED keeps two)
 };
 
 struct Bars {
@@ -380,11 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
             const int b = lt & 1;
             const bool ok = mbar_wait(bars.acc2full + 8 * b, (uint32_t)(lt >> 1) & 1u, abort_flag,
                                       a.err, lim);
-            if (issuer) bulk_wait_group_read<0>();
+            // two staging tiles: this one is free once the stores of tile lt - 2 have read it
+            if (issuer) bulk_wait_group_read<1>();
             if (named_barrier_or(2, 32 * kOutWarps, !ok)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc2_col + (uint32_t)b * (uint32_t)a.K;
-            const uint32_t dst = base_s + a.off_out;
+            const uint32_t dst = base_s + a.off_out + (uint32_t)b * a.out_bytes;
             acc_to_smem<T>(taddr, a.K, s2_s, b2_s, a.act2, dst, row);
             tc_fence_before();
             fence_proxy_async_smem();
@@ -430,7 +432,7 @@ EncodeTiledFn encode_fn() {
 uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 
 struct Layout {
-    uint32_t off_w1, off_w2, off_a2, off_out, off_in, off_sb, off_bar, plane_bytes,
+    uint32_t off_w1, off_w2, off_a2, off_out, off_in, off_sb, off_bar, out_bytes, plane_bytes,
         in_stage_bytes, in_stage_stride, w1_bytes, w2_bytes, total;
     int stages;
 };
@@ -442,7 +444,8 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
     L.w1_bytes = (uint32_t)(ks * ks * nkb_in * cm) * 128u;
     L.w2_bytes = mode == FUSED ? (uint32_t)(nkb_mid * K) * 128u : 0u;
     const uint32_t a2 = mode == FUSED ? 2u * (uint32_t)nkb_mid * kBlk : 0u;
-    const uint32_t out = (uint32_t)(((mode == FUSED ? K : cm) + 63) / 64) * kBlk;
+    L.out_bytes = (uint32_t)(((mode == FUSED ? K : cm) + 63) / 64) * kBlk;
+    const uint32_t out = (mode == FUSED ? 2u : 1u) * L.out_bytes;
     L.off_w1 = 0;
     L.off_w2 = align_up(L.w1_bytes, 1024);
     L.off_a2 = align_up(L.off_w2 + L.w2_bytes, 1024);
@@ -653,6 +656,7 @@ cudaError_t launch_tc_b2b(const fcm_handle *h, int mode_in, const void *in, void
     a.off_w2 = L.off_w2;
     a.off_a2 = L.off_a2;
     a.off_out = L.off_out;
+    a.out_bytes = L.out_bytes;
     a.off_in = L.off_in;
     a.off_sb = L.off_sb;
     a.off_bar = L.off_bar;
