@@ -57,6 +57,14 @@ static fcm_status fetch(std::vector<unsigned char> &dst, const void *src, size_t
 
 static void free_handle(fcm_handle *h) {
     if (!h) return;
+    for (int i = 0; i < 8; i++) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_run[i]) cudaEventDestroy(h->ev_run[i]);
+        if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+    }
+    if (h->ev_start) cudaEventDestroy(h->ev_start);
+    if (h->copy_in) cudaStreamDestroy(h->copy_in);
+    if (h->copy_out) cudaStreamDestroy(h->copy_out);
     void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->s1, h->b1,
                     h->s2, h->b2, h->d_err, h->mid_buf, h->stage_in, h->stage_out};
     for (void *p : ptrs)
@@ -277,6 +285,31 @@ fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, void *str
     return run_one(h, mode, in, out, s);
 }
 
+// A handle restricted to images [n0, n0 + nc) of the batch: the same weights and plan, with the
+// batch size and the tile counts of the sub-batch (callers offset the activation pointers).
+static fcm_handle batch_view(const fcm_handle *h, int nc) {
+    fcm_handle v = *h;
+    const int n = h->d.n;
+    v.d.n = nc;
+    v.x_elems = h->x_elems / n * nc;
+    v.m_elems = h->m_elems / n * nc;
+    v.y_elems = h->y_elems / n * nc;
+    for (TcPlan *p : {&v.tc, &v.tc2}) {
+        if (p->num_tiles <= 0) continue;
+        p->num_tiles = p->num_tiles / n * nc;
+        p->ctas = (int)(p->num_tiles < h->num_sms ? p->num_tiles : h->num_sms);
+    }
+    v.plan.num_tiles = h->plan.num_tiles / n * nc;
+    v.mid_buf = nullptr;
+    return v;
+}
+
+// Chunks of the batch for the pipelined host path: up to 8, as even as possible.
+static int host_chunks(const fcm_handle *h, int mode) {
+    if (mode == FCM_MODE_UNFUSED || h->d.n < 2) return 1;
+    return h->d.n < 8 ? h->d.n : 8;
+}
+
 fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
                         void *stream) {
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
@@ -301,10 +334,54 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
         h->stage_out_bytes = out_b;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    FCM_CUDA(cudaMemcpyAsync(h->stage_in, host_in, in_b, cudaMemcpyHostToDevice, s));
-    fcm_status st = fcm_run(h, mode, h->stage_in, h->stage_out, stream);
-    if (st != FCM_OK) return st;
-    FCM_CUDA(cudaMemcpyAsync(host_out, h->stage_out, out_b, cudaMemcpyDeviceToHost, s));
+    const int nch = host_chunks(h, mode);
+    if (nch == 1) {
+        FCM_CUDA(cudaMemcpyAsync(h->stage_in, host_in, in_b, cudaMemcpyHostToDevice, s));
+        fcm_status st = fcm_run(h, mode, h->stage_in, h->stage_out, stream);
+        if (st != FCM_OK) return st;
+        FCM_CUDA(cudaMemcpyAsync(host_out, h->stage_out, out_b, cudaMemcpyDeviceToHost, s));
+        FCM_CUDA(cudaStreamSynchronize(s));
+        return FCM_OK;
+    }
+    // Pipelined over chunks of the batch: the input copy of chunk i+1 (copy_in stream), the
+    // kernel of chunk i (the caller's stream) and the output copy of chunk i-1 (copy_out
+    // stream) overlap; events order each chunk's copy -> kernel -> copy.
+    if (!h->copy_in) {
+        FCM_CUDA(cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking));
+        FCM_CUDA(cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking));
+        FCM_CUDA(cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming));
+        for (int i = 0; i < 8; i++) {
+            FCM_CUDA(cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming));
+            FCM_CUDA(cudaEventCreateWithFlags(&h->ev_run[i], cudaEventDisableTiming));
+            FCM_CUDA(cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming));
+        }
+    }
+    // the copies start after the work already queued on the caller's stream
+    FCM_CUDA(cudaEventRecord(h->ev_start, s));
+    FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0));
+    FCM_CUDA(cudaStreamWaitEvent(h->copy_out, h->ev_start, 0));
+    const int n = h->d.n;
+    const size_t in_img = in_b / n, out_img = out_b / n;
+    int n0 = 0;
+    for (int i = 0; i < nch; i++) {
+        const int nc = n / nch + (i < n % nch ? 1 : 0);
+        const char *hin = static_cast<const char *>(host_in) + (size_t)n0 * in_img;
+        char *hout = static_cast<char *>(host_out) + (size_t)n0 * out_img;
+        char *din = static_cast<char *>(h->stage_in) + (size_t)n0 * in_img;
+        char *dout = static_cast<char *>(h->stage_out) + (size_t)n0 * out_img;
+        FCM_CUDA(cudaMemcpyAsync(din, hin, (size_t)nc * in_img, cudaMemcpyHostToDevice, h->copy_in));
+        FCM_CUDA(cudaEventRecord(h->ev_in[i], h->copy_in));
+        FCM_CUDA(cudaStreamWaitEvent(s, h->ev_in[i], 0));
+        fcm_handle v = batch_view(h, nc);
+        fcm_status st = run_one(&v, mode, din, dout, s);
+        if (st != FCM_OK) return st;
+        FCM_CUDA(cudaEventRecord(h->ev_run[i], s));
+        FCM_CUDA(cudaStreamWaitEvent(h->copy_out, h->ev_run[i], 0));
+        FCM_CUDA(cudaMemcpyAsync(hout, dout, (size_t)nc * out_img, cudaMemcpyDeviceToHost, h->copy_out));
+        FCM_CUDA(cudaEventRecord(h->ev_out[i], h->copy_out));
+        n0 += nc;
+    }
+    FCM_CUDA(cudaStreamWaitEvent(s, h->ev_out[nch - 1], 0));
     FCM_CUDA(cudaStreamSynchronize(s));
     return FCM_OK;
 }

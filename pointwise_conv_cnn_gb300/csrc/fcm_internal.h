@@ -58,6 +58,10 @@ struct fcm_handle {
     size_t mid_bytes = 0;
     void *stage_in = nullptr, *stage_out = nullptr;  // fcm_run_host staging
     size_t stage_in_bytes = 0, stage_out_bytes = 0;
+    // fcm_run_host pipelining: copy streams and per-chunk events (created on first use)
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t ev_start = nullptr;
+    cudaEvent_t ev_in[8] = {}, ev_run[8] = {}, ev_out[8] = {};
 };
 
 // thread-local last-error message (fcm_api.cu)

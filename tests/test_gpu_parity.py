@@ -194,6 +194,24 @@ def test_run_host_matches_run(cuda):
     assert np.array_equal(y_h.numpy(), got)
 
 
+@pytest.mark.parametrize("name,n", [("mobilenet_dwpw_f16", 5), ("b2b_dense3x3_f16", 3),
+                                    ("pwdw_f16", 9), ("tiny_dwpw_f32", 1)])
+def test_run_host_pipelined_chunks(cuda, name, n):
+    """fcm_run_host splits the batch into chunks whose copies overlap the kernels (uneven
+    chunks for n = 5 and 9): the result equals fcm_run on the device for every mode."""
+    import torch
+    wl = wk.BY_NAME[name].with_(n=n, h=min(wk.BY_NAME[name].h, 20), w=min(wk.BY_NAME[name].w, 20))
+    case = wk.make_case(wl)
+    mod = make_module(case)
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
+    x_h = to_device(case.x, wl.dtype, "cpu").pin_memory()
+    for mode, out_key in (("fused", "y"), ("conv1", "m"), ("unfused", "y")):
+        want, _ = run_case(case, mode, module=mod)
+        got = torch.full(wl.shapes()[out_key], float("nan"), dtype=tdt).pin_memory()
+        mod.run_host(x_h, got, mode)
+        assert np.array_equal(to_host(got, wl.dtype), want), mode
+
+
 def test_argument_errors(cuda):
     import torch
     wl = reduced(wk.BY_NAME["mobilenet_dwpw_f16"], n=1)
