@@ -23,6 +23,9 @@
  * that a block never needs another block's intermediate.
  *
  * Conventions for every entry point:
+ *  - A handle may be used from one host thread at a time (fcm_run_host and the first
+ *    FCM_MODE_UNFUSED run keep per-handle buffers and streams); different handles are
+ *    independent.
  *  - Status codes only: no exception, abort or exit crosses the ABI.  A human-readable
  *    message for the last failure on the calling thread is returned by fcm_last_error().
  *  - Activations are NHWC, contiguous, of the handle's dtype, 16-byte aligned, in device
@@ -141,8 +144,11 @@ FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, v
 
 /* End-to-end variant of fcm_run on HOST buffers: copies `host_in` to a device staging buffer
  * owned by the handle (allocated on first use), runs `mode`, copies the result to `host_out`
- * and synchronizes `stream` before returning.  Pinned host memory makes the copies faster;
- * pageable memory also works. */
+ * and synchronizes `stream` before returning.  For batches of two or more images (all modes
+ * but FCM_MODE_UNFUSED) the batch is split into up to 8 chunks whose input copies, kernels (on
+ * `stream`) and output copies overlap, using two copy streams the handle creates on first
+ * use.  Pinned host memory makes the copies faster and lets them overlap; pageable memory
+ * also works. */
 FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
                         void *stream);
 

@@ -96,3 +96,24 @@ def test_fused_saving_closed_forms():
         io_f = b["x"] + b["y"]
         io_u = io_f + 2 * b["mid"]
         assert abs((1 - io_f / io_u) - saving) < 1e-12, name
+
+
+def test_pwdw_plan_models_match_literal():
+    """The PWDW module's plan reports Eq. 2 + Eq. 3 layer by layer (the 1x1 over H x W, the
+    depthwise over its output) and Eq. 4 fused, for the plan's own tile, as printed."""
+    wl = wk.BY_NAME["pwdw_f16"]
+    info = fcm.fcm_plan_desc(fcm.desc_from_workload(wl))
+    H, W, C, Cm, k, s = wl.h, wl.w, wl.c, wl.cm, wl.ksize, wl.stride
+    Ho, Wo, th, tw = info["ho"], info["wo"], info["tile_h"], info["tile_w"]
+    ov = pm.overlap(W, H, tw * s, th * s, k, k, s)
+    w1, wd = Cm * C, Cm * k * k
+    lbl = (pm.pw_gma(w1, w1, H * W * C, H * W * Cm, th * tw * Cm)
+           + pm.dw_gma(Cm, ov, H * W * Cm, Ho * Wo * Cm, Ho * Wo, th * tw, wd))
+    fused = pm.pwdw_gma(C, ov, H * W * C, w1, w1, wd, wd, Ho * Wo * Cm, th * tw * Cm, Ho * Wo,
+                        th * tw)
+    e = wl.esize
+    assert info["overlap_elems"] == ov
+    assert info["gma_lbl_model"] == lbl * wl.n * e
+    assert info["gma_fused_model"] == fused * wl.n * e
+    # the intermediate (N x H x W x Cm) is what fusion keeps out of HBM
+    assert info["bytes_unfused_min"] - info["bytes_fused_min"] == 2 * wl.n * H * W * Cm * e
