@@ -32,7 +32,7 @@
  *    memory owned by the caller (except fcm_run_host, which takes host memory).
  *  - Scales and biases are float32.  Weights are of the handle's dtype.
  *  - Arithmetic: products and sums in fp32 (fp16/bf16 storage widened exactly); the
- *    intermediate is rounded to the storage dtype (round to nearest even) before the 1x1
+ *    intermediate is rounded to the storage dtype (round to nearest even) before the second
  *    convolution consumes it; the output is rounded to the storage dtype.
  *  - Zero padding, cross-correlation (no filter flip):
  *    Ho = (H + 2*pad - ksize) / stride + 1, likewise Wo.
