@@ -94,3 +94,25 @@ def test_create_without_gpu_reports_no_device(lib):
         fcm.fcm_create(good_desc(), w.ctypes.data, w.ctypes.data, w.ctypes.data, w.ctypes.data,
                        w.ctypes.data, w.ctypes.data)
     assert e.value.status == 8
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package (binding, build, workloads, CUDA sources) neither imports nor links the
+    oracle, and a missing library raises instead of falling back to anything."""
+    import subprocess
+    import sys
+    pkg = os.path.dirname(fcm.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "fcm_oracle" not in text, f
+    code = ("import sys, pointwise_conv_cnn_gb300 as fcm, pointwise_conv_cnn_gb300.workloads; "
+            "assert 'oracle' not in sys.modules; "
+            "fcm._lib = None\n"
+            "try:\n    fcm.load_library('/nonexistent/libfcm.so')\n"
+            "except FileNotFoundError:\n    print('raised')\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         cwd=os.path.dirname(pkg))
+    assert out.returncode == 0 and "raised" in out.stdout, out.stderr
