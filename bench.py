@@ -68,7 +68,7 @@ def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "pointwise_conv_cnn_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if (f.startswith("tc_") and f.endswith(".cu")) or f in ("tc_common.cuh", "fcm_device.cuh"):
+        if f.startswith("tc_") or f == "fcm_device.cuh":
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
