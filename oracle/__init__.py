@@ -7,7 +7,9 @@ from it.
 
 The arithmetic lives in ``fcm_oracle.c`` (plain loops, fp64).  This module only builds that
 file with gcc, loads it with ctypes and marshals numpy arrays.  Inputs of any float dtype are
-upcast to float64 exactly before the call; outputs are float64.
+upcast to float64 exactly before the call; outputs are float64.  The INT8 functions
+(``dw_i8``, ``pw_i8``, ``fused_i8``) take int8 activations and weights and fp32 scales and
+biases, and return int8 (section III-B's INT8 FCMs).
 
 Definitions followed (see the C file for the full list): "Fusing Depthwise and Pointwise
 Convolutions for Efficient Inference on GPUs", section II-B (DW and PW convolutions),
@@ -60,8 +62,15 @@ def bind(path: str):
     lib.oracle_round_format.argtypes = [ctypes.c_double, i, i, ctypes.c_double]
     lib.oracle_round_format.restype = ctypes.c_double
     lib.oracle_max_threads.argtypes = [i]
+    bp = ctypes.POINTER(ctypes.c_int8)
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_dw_i8.argtypes = [i] * 7 + [bp, bp, fp, fp, i, bp, i]
+    lib.oracle_pw_i8.argtypes = [i] * 5 + [bp, bp, fp, fp, i, bp, i]
+    lib.oracle_fused_i8.argtypes = [i] * 8 + [bp, bp, fp, fp, i, bp, fp, fp, i, bp, i]
+    lib.oracle_requant_i8.argtypes = [ctypes.c_longlong, ctypes.c_float, ctypes.c_float, i]
     for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused, lib.oracle_pwdw,
-              lib.oracle_max_threads):
+              lib.oracle_max_threads, lib.oracle_dw_i8, lib.oracle_pw_i8, lib.oracle_fused_i8,
+              lib.oracle_requant_i8):
         f.restype = ctypes.c_int
     return lib
 
@@ -181,6 +190,84 @@ def pwdw(x, wq, s1, b1, wd2, s2, b2, act1="none", act2="none", stride=1, pad=0, 
                                 MID[mid], _ptr(y), nthreads)
     if rc != 0:
         raise ValueError("oracle_pwdw: invalid shape")
+    return y
+
+
+def _i8(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.int8:
+        if not np.issubdtype(a.dtype, np.integer) or a.min(initial=0) < -128 or a.max(initial=0) > 127:
+            raise ValueError("int8 operand expected")
+        a = a.astype(np.int8)
+    return np.ascontiguousarray(a)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _p8(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
+
+
+def _p32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def requant_i8(acc: int, s: float, b: float, act: str = "none", lib=None) -> int:
+    """int8 requantization of one accumulator: clamp(rint(act(fma32(s, acc, b))), -128, 127)."""
+    return int(_load(lib).oracle_requant_i8(int(acc), float(s), float(b), ACT[act]))
+
+
+def dw_i8(x, wd, s1, b1, act1="none", stride=1, pad=0, nthreads=0, lib=None) -> np.ndarray:
+    """INT8 depthwise conv: x [N,H,W,C] int8, wd [C,k,k] int8, s1/b1 fp32 -> m int8."""
+    x, wd = _i8(x), _i8(wd)
+    s1, b1 = _f32(s1), _f32(b1)
+    N, H, W, C = x.shape
+    k = wd.shape[1]
+    assert wd.shape == (C, k, k) and s1.shape == (C,) and b1.shape == (C,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    m = np.empty((N, Ho, Wo, C), np.int8)
+    rc = _load(lib).oracle_dw_i8(N, H, W, C, k, stride, pad, _p8(x), _p8(wd), _p32(s1),
+                                 _p32(b1), ACT[act1], _p8(m), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_dw_i8: invalid shape")
+    return m
+
+
+def pw_i8(m, wp, s2, b2, act2="none", nthreads=0, lib=None) -> np.ndarray:
+    """INT8 pointwise conv: m [N,Ho,Wo,Cm] int8, wp [K,Cm] int8, s2/b2 fp32 -> y int8."""
+    m, wp = _i8(m), _i8(wp)
+    s2, b2 = _f32(s2), _f32(b2)
+    N, Ho, Wo, Cm = m.shape
+    K = wp.shape[0]
+    assert wp.shape == (K, Cm) and s2.shape == (K,) and b2.shape == (K,)
+    y = np.empty((N, Ho, Wo, K), np.int8)
+    rc = _load(lib).oracle_pw_i8(N, Ho, Wo, Cm, K, _p8(m), _p8(wp), _p32(s2), _p32(b2),
+                                 ACT[act2], _p8(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pw_i8: invalid shape")
+    return y
+
+
+def fused_i8(x, wd, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1, pad=0,
+             nthreads=0, lib=None) -> np.ndarray:
+    """INT8 DW -> PW module in one pass (int8 intermediate): x [N,H,W,C], wd [C,k,k],
+    wp [K,C] int8; s1/b1 [C], s2/b2 [K] fp32 -> y [N,Ho,Wo,K] int8."""
+    x, wd, wp = _i8(x), _i8(wd), _i8(wp)
+    s1, b1, s2, b2 = map(_f32, (s1, b1, s2, b2))
+    N, H, W, C = x.shape
+    k = wd.shape[1]
+    K = wp.shape[0]
+    assert wd.shape == (C, k, k) and wp.shape == (K, C)
+    assert s1.shape == (C,) and b1.shape == (C,) and s2.shape == (K,) and b2.shape == (K,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    y = np.empty((N, Ho, Wo, K), np.int8)
+    rc = _load(lib).oracle_fused_i8(N, H, W, C, K, k, stride, pad, _p8(x), _p8(wd), _p32(s1),
+                                    _p32(b1), ACT[act1], _p8(wp), _p32(s2), _p32(b2), ACT[act2],
+                                    _p8(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_fused_i8: invalid shape")
     return y
 
 

@@ -292,3 +292,132 @@ int oracle_pwdw(int N, int H, int W, int C, int Cm, int k, int s, int p,
                 }
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * INT8 module (section III-B: INT8 feature maps and weights, four-way int8 products with
+ * 32-bit accumulation, every buffer -- the commBuffer included -- holding int8 values packed
+ * four to a word; weights packed offline).  The pages give no quantization scheme, so the
+ * plainest one is read (and listed in the design notes):
+ *  - x, the filters, the intermediate m and the output y are int8; a convolution's
+ *    accumulator is the exact integer sum of int8 x int8 products;
+ *  - the folded norm is a per-channel fp32 scale and bias, applied to the accumulator as one
+ *    fp32 fused multiply-add, v = fma(s, (float)acc, b) (|acc| < 2^24 for every supported
+ *    shape, so the conversion is exact); this is the precision in which the GPU takes the
+ *    rounding decision, so the oracle takes it in the same one;
+ *  - then the activation, rounding to the nearest integer (ties to even) and saturation to
+ *    [-128, 127]: q = clamp(rint(act(v)), -128, 127).
+ * The accumulators are int64 here, so nothing can overflow.
+ * Layouts as above: x [N][H][W][C], wd [C][k][k], wp [K][C], m [N][Ho][Wo][C],
+ * y [N][Ho][Wo][K]; s and b are float32.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Requantization of one accumulator to int8. */
+static int8_t requant_i8(int64_t acc, float s, float b, int act) {
+    float v = fmaf(s, (float)acc, b);
+    double a = act_apply((double)v, act);
+    double r = nearbyint(a); /* default rounding mode: to nearest, ties to even */
+    if (r < -128.0) r = -128.0;
+    if (r > 127.0) r = 127.0;
+    return (int8_t)r;
+}
+
+/* Requantization of one value, exposed for the tests' closed-form checks. */
+int oracle_requant_i8(long long acc, float s, float b, int act) {
+    return (int)requant_i8((int64_t)acc, s, b, act);
+}
+
+/* INT8 depthwise k x k convolution + requantization (section II-B, section III-B INT8). */
+int oracle_dw_i8(int N, int H, int W, int C, int k, int s, int p,
+                 const int8_t *x, const int8_t *wd, const float *s1, const float *b1, int act1,
+                 int8_t *m, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int c = 0; c < C; c++) {
+                    int64_t t = 0;
+                    for (int i = 0; i < k; i++) {
+                        int hi = ho * s - p + i;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int j = 0; j < k; j++) {
+                            int wi = wo * s - p + j;
+                            if (wi < 0 || wi >= W) continue;
+                            t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *
+                                 (int64_t)wd[((size_t)c * k + i) * k + j];
+                        }
+                    }
+                    m[IDX4(n, ho, wo, c, Ho, Wo, C)] = requant_i8(t, s1[c], b1[c], act1);
+                }
+    return 0;
+}
+
+/* INT8 pointwise 1x1 convolution + requantization. */
+int oracle_pw_i8(int N, int Ho, int Wo, int Cm, int K,
+                 const int8_t *m, const int8_t *wp, const float *s2, const float *b2, int act2,
+                 int8_t *y, int nthreads) {
+    if (N < 0 || Ho < 1 || Wo < 1 || Cm < 1 || K < 1) return -1;
+    set_threads(nthreads);
+    long long P = (long long)N * Ho * Wo;
+#pragma omp parallel for schedule(static)
+    for (long long q = 0; q < P; q++)
+        for (int kk = 0; kk < K; kk++) {
+            int64_t t = 0;
+            for (int c = 0; c < Cm; c++)
+                t += (int64_t)m[(size_t)q * Cm + c] * (int64_t)wp[(size_t)kk * Cm + c];
+            y[(size_t)q * K + kk] = requant_i8(t, s2[kk], b2[kk], act2);
+        }
+    return 0;
+}
+
+/* The INT8 DW -> PW module as its own single pass (one output pixel at a time: its int8
+ * intermediate vector over all channels, then the 1x1 convolution of it).  It does not call
+ * oracle_dw_i8/oracle_pw_i8. */
+int oracle_fused_i8(int N, int H, int W, int C, int K, int k, int s, int p,
+                    const int8_t *x, const int8_t *wd, const float *s1, const float *b1, int act1,
+                    const int8_t *wp, const float *s2, const float *b2, int act2,
+                    int8_t *y, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || K < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        int8_t *mid = (int8_t *)malloc((size_t)C);
+        if (!mid) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for collapse(2) schedule(static)
+        for (int n = 0; n < N; n++)
+            for (int ho = 0; ho < Ho; ho++) {
+                if (!mid) continue;
+                for (int wo = 0; wo < Wo; wo++) {
+                    for (int c = 0; c < C; c++) {
+                        int64_t t = 0;
+                        for (int i = 0; i < k; i++) {
+                            int hi = ho * s - p + i;
+                            if (hi < 0 || hi >= H) continue;
+                            for (int j = 0; j < k; j++) {
+                                int wi = wo * s - p + j;
+                                if (wi < 0 || wi >= W) continue;
+                                t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *
+                                     (int64_t)wd[((size_t)c * k + i) * k + j];
+                            }
+                        }
+                        mid[c] = requant_i8(t, s1[c], b1[c], act1);
+                    }
+                    for (int kk = 0; kk < K; kk++) {
+                        int64_t t = 0;
+                        for (int c = 0; c < C; c++)
+                            t += (int64_t)mid[c] * (int64_t)wp[(size_t)kk * C + c];
+                        y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], b2[kk], act2);
+                    }
+                }
+            }
+        free(mid);
+    }
+    return failed ? -1 : 0;
+}
