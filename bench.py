@@ -143,7 +143,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ our path
 def torch_dtype(torch, dtype):
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+            "i8": torch.int8}[dtype]
+
+
+def oracle_step(oracle, wk, wl, case):
+    """One evaluation of the oracle's single-pass module on `case` (fp64, or the INT8 one)."""
+    if wl.dtype == "i8":
+        return lambda: oracle.fused_i8(case.x, case.w1, case.s1, case.b1, case.wp, case.s2,
+                                       case.b2, wl.act1, wl.act2, wl.stride, wl.pad)
+    f = case.f64()
+    return lambda: oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
+                                wl.act1, wl.act2, wl.stride, wl.pad, conv1=wl.conv1)
 
 
 def storage_tensor(torch, arr, dtype):
@@ -237,11 +248,10 @@ def cpu_baseline(wk, wl, seconds: float) -> dict:
 
     def timed(n_img, reps):
         sub = wl.with_(n=n_img)
-        f = wk.make_case(sub).f64()
+        run = oracle_step(oracle, wk, sub, wk.make_case(sub))
         t = time.perf_counter()
         for _ in range(reps):
-            oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"], wl.act1,
-                         wl.act2, wl.stride, wl.pad, conv1=wl.conv1)
+            run()
         return time.perf_counter() - t
 
     t1 = timed(1, 1)
@@ -251,8 +261,9 @@ def cpu_baseline(wk, wl, seconds: float) -> dict:
     ips = n_img * reps / t
     return {"value": round(ips * per_image_bytes / 1e9, 6), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "images_per_s": round(ips, 4),
-            "sample": f"{n_img} of {wl.n} images of {wl.name} x {reps} passes, fp64 "
-                      f"oracle_fused, {threads} OpenMP threads, {t:.2f} s"}
+            "sample": f"{n_img} of {wl.n} images of {wl.name} x {reps} passes, "
+                      f"{'INT8 oracle_fused_i8' if wl.dtype == 'i8' else 'fp64 oracle_fused'}, "
+                      f"{threads} OpenMP threads, {t:.2f} s"}
 
 
 # ------------------------------------------------------------------ multi-rank aggregation
@@ -313,7 +324,8 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(region_ms / steps, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"i8": "int8"}.get(wl.dtype, wl.dtype),
         "data": DATA,
         "config": {"workload": wl.name, "n": wl.n, "h": wl.h, "w": wl.w, "c": wl.c,
                    "k_out": wl.k_out, "conv1": wl.conv1, "ksize": wl.ksize, "stride": wl.stride,
@@ -354,7 +366,7 @@ def report_all(torch, fcm, wk, device):
     for wl in wk.WORKLOADS:
         for mode in ("fused", "unfused"):
             for kernel in ("auto", "simt"):
-                if kernel == "simt" and wl.dtype == "f32":
+                if kernel == "simt" and wl.dtype in ("f32", "i8"):   # f32: SIMT only; i8: TC only
                     continue
                 steps = 200 if wl.n > 1 else 2000
                 try:
@@ -391,12 +403,7 @@ def run_reference(args):
     threads = oracle.max_threads()
     n_img = 1 if wl.n > 1 else wl.n
     sub = wl.with_(n=n_img)
-    case = wk.make_case(sub)
-    f = case.f64()
-
-    def step():
-        oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"], wl.act1,
-                     wl.act2, wl.stride, wl.pad, conv1=wl.conv1)
+    step = oracle_step(oracle, wk, sub, wk.make_case(sub))
 
     for _ in range(args.warmup):
         step()
@@ -409,14 +416,16 @@ def run_reference(args):
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "int8" if wl.dtype == "i8" else "f64", "data": DATA,
            "config": {"workload": wl.name, "n": wl.n, "h": wl.h, "w": wl.w, "c": wl.c,
                       "k_out": wl.k_out, "images_per_step": n_img},
            "images_per_s": round(n_img / dt, 4),
            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": threads,
                             "kind": "oracle",
                             "sample": f"{n_img} image(s) of {wl.n} per step of {wl.name}, "
-                                      f"fp64 oracle_fused, {threads} OpenMP threads"},
+                                      f"{'INT8' if wl.dtype == 'i8' else 'fp64'} oracle, "
+                                      f"{threads} OpenMP threads"},
            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

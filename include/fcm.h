@@ -33,7 +33,8 @@
  *  - Scales and biases are float32.  Weights are of the handle's dtype.
  *  - Arithmetic: products and sums in fp32 (fp16/bf16 storage widened exactly); the
  *    intermediate is rounded to the storage dtype (round to nearest even) before the second
- *    convolution consumes it; the output is rounded to the storage dtype.
+ *    convolution consumes it; the output is rounded to the storage dtype.  INT8: exact
+ *    integer sums, then the requantization described at fcm_dtype.
  *  - Zero padding, cross-correlation (no filter flip):
  *    Ho = (H + 2*pad - ksize) / stride + 1, likewise Wo.
  */
@@ -64,7 +65,16 @@ typedef enum fcm_status {
     FCM_ERR_NO_DEVICE = 8      /* no CUDA device, or not a compute capability 10.3 device */
 } fcm_status;
 
-typedef enum fcm_dtype { FCM_F32 = 0, FCM_F16 = 1, FCM_BF16 = 2 } fcm_dtype;
+/* Storage types.  FCM_I8 is the INT8 module of the paper's section III-B (int8 feature maps
+ * and weights, 32-bit integer accumulation, int8 intermediate): every activation, weight and
+ * the intermediate are int8; scales and biases stay float32 and requantize each accumulator,
+ *     q = clamp(rint(act(fmaf(s, (float)acc, b))), -128, 127)      (rint: ties to even),
+ * the fma and the rounding in fp32 (|acc| < 2^24 for every supported shape, so acc converts
+ * exactly).  INT8 runs only the depthwise module (FCM_CONV1_DEPTHWISE) on the tensor-core
+ * kernels (C and K multiples of 16, K <= 256, ksize 1/3/5/7); other INT8 requests return
+ * FCM_ERR_UNSUPPORTED.  The results are exact: the same integers on every run and in every
+ * mode. */
+typedef enum fcm_dtype { FCM_F32 = 0, FCM_F16 = 1, FCM_BF16 = 2, FCM_I8 = 3 } fcm_dtype;
 typedef enum fcm_act { FCM_ACT_NONE = 0, FCM_ACT_RELU = 1, FCM_ACT_RELU6 = 2 } fcm_act;
 /* The module's layer pair.  DEPTHWISE and DENSE: a k x k first convolution, then 1x1.
  * POINTWISE (PWDW): a 1x1 first convolution C -> Cm (Cm = mid, or C when mid is 0), then a

@@ -32,7 +32,7 @@ FCM_OK = 0
 STATUS_NAMES = {0: "FCM_OK", 1: "FCM_ERR_INVALID_ARG", 2: "FCM_ERR_UNSUPPORTED",
                 3: "FCM_ERR_ALIGNMENT", 4: "FCM_ERR_SMEM_BUDGET", 5: "FCM_ERR_CUDA",
                 6: "FCM_ERR_TIMEOUT", 7: "FCM_ERR_DEVICE_FAULT", 8: "FCM_ERR_NO_DEVICE"}
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3}
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
 CONV1 = {"dw": 0, "dense": 1, "pwdw": 2}
 MODES = {"fused": 0, "conv1": 1, "pw": 2, "unfused": 3}
@@ -260,7 +260,7 @@ def fcm_fuse_plan(layers, batch: int = 1, num_sms: int = 152, l1_bytes: int = 23
 
 class FusedConvModule:
     """Owns one FCM handle.  Weights are torch tensors or numpy arrays in the storage dtype
-    (bf16 may be given as uint16 bit patterns); scales/biases float32."""
+    (bf16 may be given as uint16 bit patterns, INT8 as int8); scales/biases float32."""
 
     def __init__(self, desc: FcmDesc, w1, wp, s1, b1, s2, b2):
         import numpy as np

@@ -35,6 +35,7 @@ static float host_to_f(const void *base, size_t i, int dtype) {
     switch (dtype) {
     case FCM_F32: return static_cast<const float *>(base)[i];
     case FCM_F16: return __half2float(static_cast<const __half *>(base)[i]);
+    case FCM_I8: return (float)static_cast<const signed char *>(base)[i];
     default: return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[i]);
     }
 }
@@ -66,7 +67,8 @@ static void free_handle(fcm_handle *h) {
     if (h->copy_in) cudaStreamDestroy(h->copy_in);
     if (h->copy_out) cudaStreamDestroy(h->copy_out);
     void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->s1, h->b1,
-                    h->s2, h->b2, h->d_err, h->mid_buf, h->stage_in, h->stage_out};
+                    h->s2, h->b2, h->q1, h->i8_one, h->i8_zero, h->i8_idq, h->i8_idtap,
+                    h->d_err, h->mid_buf, h->stage_in, h->stage_out};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete h;
@@ -81,7 +83,7 @@ fcm_status fcm_tensor_bytes(const fcm_desc *desc, size_t *x_bytes, size_t *m_byt
     int ho, wo, cm;
     fcm_status st = fcm_validate_desc(desc, &ho, &wo, &cm);
     if (st != FCM_OK) return st;
-    size_t e = desc->dtype == FCM_F32 ? 4 : 2;
+    size_t e = (size_t)fcm_dtype_bytes(desc->dtype);
     if (x_bytes) *x_bytes = (size_t)desc->n * desc->h * desc->w * desc->c * e;
     const bool pwdw = desc->conv1 == FCM_CONV1_POINTWISE;   // m keeps the input's extent
     if (m_bytes) *m_bytes = (size_t)desc->n * (pwdw ? desc->h : ho) * (pwdw ? desc->w : wo) * cm * e;
@@ -126,7 +128,7 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
     h->ho = ho;
     h->wo = wo;
     h->cm = cm;
-    h->esize = desc->dtype == FCM_F32 ? 4 : 2;
+    h->esize = fcm_dtype_bytes(desc->dtype);
     h->num_sms = prop.multiProcessorCount;
     h->smem_optin = (int)prop.sharedMemPerBlockOptin;
     h->x_elems = (size_t)desc->n * desc->h * desc->w * desc->c;

@@ -7,6 +7,9 @@
 
 #include "../../include/fcm.h"
 
+// Bytes of one element of a storage type.
+inline int fcm_dtype_bytes(int dtype) { return dtype == FCM_F32 ? 4 : dtype == FCM_I8 ? 1 : 2; }
+
 // Device error word bits, written by kernels with atomicOr and read by fcm_check.
 enum : unsigned {
     FCM_DEVERR_TIMEOUT = 1u,   // a bounded mbarrier wait gave up
@@ -35,7 +38,8 @@ struct fcm_handle {
     fcm_desc d{};
     fcm_plan_info plan{};
     TcPlan tc{};
-    TcPlan tc2{};             // PWDW: plan of the layer-by-layer depthwise stage
+    TcPlan tc2{};             // PWDW: plan of the layer-by-layer depthwise stage;
+                              // INT8: plan of the PW-only stage (identity stencil, k = 1)
     int device = -1;
     int ho = 0, wo = 0, cm = 0;
     int esize = 0;
@@ -50,8 +54,13 @@ struct fcm_handle {
     size_t wp_img_bytes = 0;
     void *w1_img = nullptr;   // tcgen05 B-operand images of dense conv1, one per tap
     size_t w1_img_bytes = 0;
-    void *w1dw_img = nullptr; // DW taps for the tcgen05 DW stage: [k*k][C], storage dtype
+    void *w1dw_img = nullptr; // DW taps for the tcgen05 DW stage: [k*k][C], storage dtype (f16 for INT8)
     float *s1 = nullptr, *b1 = nullptr, *s2 = nullptr, *b2 = nullptr;
+    // INT8: 1152 * (sum of each channel's taps), and the identity stencil (one f16 tap of 1,
+    // scale 1, bias 0, offset 1152) through which the PW-only mode runs on the fused kernel
+    float *q1 = nullptr;
+    float *i8_one = nullptr, *i8_zero = nullptr, *i8_idq = nullptr;
+    void *i8_idtap = nullptr;
     unsigned *d_err = nullptr;
 
     void *mid_buf = nullptr;  // FCM_MODE_UNFUSED intermediate (lazily allocated)

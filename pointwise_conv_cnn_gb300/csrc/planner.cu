@@ -67,8 +67,10 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
     if (d->conv1 != FCM_CONV1_DEPTHWISE && d->conv1 != FCM_CONV1_DENSE &&
         d->conv1 != FCM_CONV1_POINTWISE)
         return fcm_fail(FCM_ERR_INVALID_ARG, "conv1 kind %d", d->conv1);
-    if (d->dtype < FCM_F32 || d->dtype > FCM_BF16)
+    if (d->dtype < FCM_F32 || d->dtype > FCM_I8)
         return fcm_fail(FCM_ERR_INVALID_ARG, "dtype %d", d->dtype);
+    if (d->dtype == FCM_I8 && d->conv1 != FCM_CONV1_DEPTHWISE)
+        return fcm_fail(FCM_ERR_UNSUPPORTED, "INT8 runs the depthwise -> pointwise module only");
     if (d->act1 < FCM_ACT_NONE || d->act1 > FCM_ACT_RELU6 || d->act2 < FCM_ACT_NONE ||
         d->act2 > FCM_ACT_RELU6)
         return fcm_fail(FCM_ERR_INVALID_ARG, "activation code out of range");
@@ -89,7 +91,7 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
     int w_o = out_extent(d->w, d->ksize, d->stride, d->pad);
     if (h_o < 1 || w_o < 1) return fcm_fail(FCM_ERR_INVALID_ARG, "empty output");
     // every NHWC row must start on a 16-byte boundary for the vector paths
-    int esize = d->dtype == FCM_F32 ? 4 : 2;
+    int esize = fcm_dtype_bytes(d->dtype);
     if (((long long)d->c * esize) % 16 != 0 || ((long long)m * esize) % 16 != 0 ||
         ((long long)d->k_out * esize) % 16 != 0)
         return fcm_fail(FCM_ERR_ALIGNMENT,
@@ -108,7 +110,7 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
 // Byte counts and the section IV cost models for an output tile of th x tw pixels.
 static void fill_bytes(const fcm_desc *d, int ho, int wo, int cm, int th, int tw,
                        fcm_plan_info *info) {
-    long long e = d->dtype == FCM_F32 ? 4 : 2;
+    long long e = fcm_dtype_bytes(d->dtype);
     long long N = d->n, H = d->h, W = d->w, C = d->c, K = d->k_out, k = d->ksize;
     const bool pwdw = d->conv1 == FCM_CONV1_POINTWISE;
     long long x = N * H * W * C, y = N * ho * wo * K;
@@ -167,6 +169,9 @@ fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm
     if (d->kernel == FCM_KERNEL_TC && !tc_ok)
         return fcm_fail(FCM_ERR_UNSUPPORTED, "tensor-core kernels requested but unavailable: %s",
                         why ? why : (d->dtype == FCM_F32 ? "fp32 runs on CUDA cores" : "no tile fits"));
+    if (d->dtype == FCM_I8 && !tc_ok)   // INT8 has no CUDA-core kernels
+        return fcm_fail(FCM_ERR_UNSUPPORTED, "INT8 needs the tensor-core kernels: %s",
+                        why ? why : (d->kernel == FCM_KERNEL_SIMT ? "SIMT requested" : "no tile fits"));
     if (tc_ok) {
         info->kernel = FCM_KERNEL_TC;
         info->tile_h = t->tile_h;

@@ -228,6 +228,51 @@ template <> struct Pack2<__nv_bfloat16> {
     }
 };
 
+// ------------------------------------------------------- INT8 storage
+// int8 values are exact in f16 and the products of two of them exact in fp32, so the INT8
+// module runs on the 16-bit paths: the tensor core multiplies f16 images of int8 operands into
+// an fp32 accumulator (exact while every partial sum stays below 2^22), and the depthwise
+// stencil uses the mixed-precision f16 FMA.
+struct I8 {
+    // Offset carried by widened inputs: 1024 (the f16 pattern 0x6400, whose ulp is 1) + 128.
+    static constexpr float kBias = 1152.0f;
+    // Four int8 lanes -> two f16x2 holding 1152 + x: the byte x ^ 0x80 = x + 128 (0..255) is
+    // placed in the low mantissa bits of 0x6400.  The stencil sums (1152 + x) * w over its taps
+    // and subtracts 1152 * (sum of the channel's taps) at the end; every step is exact.
+    static __device__ __forceinline__ void widen4(uint32_t x4, uint32_t &lo, uint32_t &hi) {
+        const uint32_t u = x4 ^ 0x80808080u;
+        lo = __byte_perm(u, 0x64646464u, 0x4140);
+        hi = __byte_perm(u, 0x64646464u, 0x4342);
+    }
+    // Requantization of v = s * acc + b: clamp to the activation's integer range (none
+    // [-128, 127], ReLU [0, 127], ReLU6 [0, 6]; clamping to integer bounds commutes with
+    // rounding), then round to the nearest integer, ties to even, by adding 1.5 * 2^23 (ulp 1
+    // there): the sum holds the integer r, and its low byte is r as an int8.
+    static constexpr float kRound = 12582912.0f;
+    template <int ACT>
+    static __device__ __forceinline__ float biased(float v) {
+        const float lo = ACT == 0 ? -128.0f : 0.0f;
+        const float hi = ACT == 2 ? 6.0f : 127.0f;
+        return __fadd_rn(fminf(fmaxf(v, lo), hi), kRound);
+    }
+    // Two requantized values as f16x2 (`lo` in the low half): the A operand of the 1x1 GEMM.
+    template <int ACT>
+    static __device__ __forceinline__ uint32_t half2(float lo, float hi) {
+        const float rl = __fsub_rn(biased<ACT>(lo), kRound);
+        const float rh = __fsub_rn(biased<ACT>(hi), kRound);
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(rh), "f"(rl));
+        return r;
+    }
+    // Four requantized values packed as int8 lanes (a in the lowest byte).
+    template <int ACT>
+    static __device__ __forceinline__ uint32_t bytes4(float a, float b, float c, float d) {
+        const uint32_t ta = __float_as_uint(biased<ACT>(a)), tb = __float_as_uint(biased<ACT>(b));
+        const uint32_t tc = __float_as_uint(biased<ACT>(c)), td = __float_as_uint(biased<ACT>(d));
+        return __byte_perm(__byte_perm(ta, tb, 0x0040), __byte_perm(tc, td, 0x0040), 0x5410);
+    }
+};
+
 // Calls f(std::integral_constant<int, act>{}) for a runtime activation code 0, 1 or 2, so that a
 // role's loop is compiled once per activation.
 template <typename F>

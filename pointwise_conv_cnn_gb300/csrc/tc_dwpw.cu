@@ -51,10 +51,13 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
                    int out_bufs) {
     Layout L{};
     const int C = cm, K = d->k_out, nkb = (C + 63) / 64;
+    const int es = fcm_dtype_bytes(d->dtype);
+    const bool i8 = d->dtype == FCM_I8;
+    // the B image and the A tile are 16-bit for every storage type (INT8 as exact f16)
     const uint32_t b_bytes = mode == DWONLY ? 0u : (uint32_t)nkb * K * 128;
     const uint32_t a_bytes = mode == FUSED ? (uint32_t)nkb * kTileM * 128 : 0u;
     const uint32_t out_bytes =
-        mode == DWONLY ? 0u : (uint32_t)(out_bufs * ((K + 63) / 64)) * kOutBlock;
+        mode == DWONLY ? 0u : (uint32_t)(out_bufs * ((K + 63) / 64)) * (uint32_t)out_block_bytes(es);
     L.off_b = 0;
     L.off_a = align_up(b_bytes, 1024);
     L.off_out = align_up(L.off_a + a_bytes, 1024);
@@ -62,10 +65,10 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
     if (mode == PWONLY)
         L.in_stage_bytes = (uint32_t)nkb * kTileM * 128;
     else
-        L.in_stage_bytes = (uint32_t)p.in_rows * p.in_cols * p.chunk_c * 2;
+        L.in_stage_bytes = (uint32_t)p.in_rows * p.in_cols * p.chunk_c * es;
     L.in_stage_stride = align_up(L.in_stage_bytes, 1024);
     const uint32_t wdw = mode == PWONLY ? 0u : (uint32_t)C * d->ksize * d->ksize * 2;
-    const uint32_t sb = (uint32_t)(2 * C + 2 * K) * 4;
+    const uint32_t sb = (uint32_t)(2 * C + 2 * K + (i8 ? C : 0)) * 4;
     const uint32_t tail = align_up(wdw, 16) + align_up(sb, 16) + kBarBytes + 16 + 1024;
     int stages = mode == PWONLY ? 4 : p.stages;
     for (; stages >= 1; stages--) {
@@ -95,6 +98,8 @@ int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why
     if (d->conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_supported(d, ho, wo, cm, why);
     if (d->conv1 != FCM_CONV1_DEPTHWISE) return fcm_b2b_supported(d, ho, wo, cm, why);
     if (cm % 16 != 0) return no("channels must be a multiple of 16");
+    // INT8: the 1x1's fp32 partial sums stay below 256 * 128 * 128 = 2^22, exact on the tensor core
+    if (d->dtype == FCM_I8 && cm > 256) return no("INT8 takes at most 256 channels");
     if (d->k_out % 16 != 0 || d->k_out < 16 || d->k_out > 256)
         return no("k_out must be a multiple of 16 in [16, 256]");
     if (d->ksize != 1 && d->ksize != 3 && d->ksize != 5 && d->ksize != 7)
@@ -191,26 +196,92 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
     return FCM_OK;
 }
 
+namespace {
+
+// INT8 handle parts: the per-channel stencil offsets 1152 * sum(taps), the identity stencil of
+// the PW-only mode and that mode's plan (the fused kernel with k = 1 over the intermediate).
+fcm_desc i8_pw_desc(const fcm_handle *h) {
+    fcm_desc v = h->d;
+    v.h = h->ho;
+    v.w = h->wo;
+    v.c = h->cm;
+    v.mid = 0;
+    v.ksize = 1;
+    v.stride = 1;
+    v.pad = 0;
+    v.act1 = FCM_ACT_NONE;
+    v.tile_h = 0;
+    v.tile_w = 0;
+    return v;
+}
+
+fcm_status prepare_i8(fcm_handle *h, const void *w1_host) {
+    const int C = h->cm, KS = h->d.ksize;
+    const signed char *w8 = static_cast<const signed char *>(w1_host);
+    std::vector<float> q1(C), one(C, 1.0f), zero(C, 0.0f), idq(C, I8::kBias);
+    for (int c = 0; c < C; c++) {
+        int sum = 0;
+        for (int t = 0; t < KS * KS; t++) sum += w8[(size_t)c * KS * KS + t];
+        q1[c] = I8::kBias * (float)sum;   // |sum| <= 49 * 128: exact
+    }
+    const __half h1 = __float2half_rn(1.0f);
+    std::vector<__half> idtap(C, h1);
+    const size_t fb = (size_t)C * sizeof(float);
+    if (cudaMalloc(&h->q1, fb) != cudaSuccess ||
+        cudaMemcpy(h->q1, q1.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_one, fb) != cudaSuccess ||
+        cudaMemcpy(h->i8_one, one.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_zero, fb) != cudaSuccess ||
+        cudaMemcpy(h->i8_zero, zero.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_idq, fb) != cudaSuccess ||
+        cudaMemcpy(h->i8_idq, idq.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_idtap, (size_t)C * 2) != cudaSuccess ||
+        cudaMemcpy(h->i8_idtap, idtap.data(), (size_t)C * 2, cudaMemcpyHostToDevice) != cudaSuccess)
+        return fcm_fail(FCM_ERR_CUDA, "INT8 stencil constants: %s",
+                        cudaGetErrorString(cudaGetLastError()));
+    const fcm_desc v = i8_pw_desc(h);
+    if (fcm_tc_plan(&v, h->ho, h->wo, C, h->num_sms, h->smem_optin, &h->tc2) != FCM_OK)
+        return fcm_fail(FCM_ERR_SMEM_BUDGET, "INT8 PW-only stage: no tile fits");
+    return FCM_OK;
+}
+
+}  // namespace
+
 fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_host) {
     if (h->d.conv1 == FCM_CONV1_DENSE) return fcm_b2b_prepare(h, w1_host, wp_host);
     if (h->d.conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_prepare(h, w1_host, wp_host);
     const fcm_desc &d = h->d;
     const int C = h->cm, K = d.k_out, KS = d.ksize, nkb = (C + 63) / 64;
+    const bool i8 = d.dtype == FCM_I8;
+    // 16-bit pattern of weight i: the storage value itself, or for INT8 the f16 of the int8
+    // value (exact)
+    auto w16 = [&](const void *base, size_t i) -> uint16_t {
+        if (i8) {
+            __half hv = __float2half_rn((float)static_cast<const signed char *>(base)[i]);
+            uint16_t b;
+            memcpy(&b, &hv, 2);
+            return b;
+        }
+        return static_cast<const uint16_t *>(base)[i];
+    };
     // B operand image: row n = output channel, K-dim = input channel, 128B swizzle
     h->wp_img_bytes = (size_t)nkb * K * 128;
     std::vector<uint8_t> img(h->wp_img_bytes, 0);
-    const uint16_t *wp16 = static_cast<const uint16_t *>(wp_host);
     for (int n = 0; n < K; n++)
         for (int c = 0; c < C; c++) {
             uint32_t off = sw128_offset(n, c, K, 2);
-            memcpy(&img[off], &wp16[(size_t)n * C + c], 2);
+            const uint16_t b = w16(wp_host, (size_t)n * C + c);
+            memcpy(&img[off], &b, 2);
         }
-    // DW taps in the storage dtype, tap-major: [k*k][C] (lane v of a warp reads channels
-    // 8v..8v+7 of one tap as one 16-byte vector, consecutive lanes consecutive vectors)
+    // DW taps in the storage dtype (f16 for INT8), tap-major: [k*k][C] (lane v of a warp reads
+    // channels 8v..8v+7 of one tap as one 16-byte vector, consecutive lanes consecutive vectors)
     std::vector<uint16_t> wdw((size_t)C * KS * KS);
-    const uint16_t *w1b = static_cast<const uint16_t *>(w1_host);
     for (int c = 0; c < C; c++)
-        for (int t = 0; t < KS * KS; t++) wdw[(size_t)t * C + c] = w1b[(size_t)c * KS * KS + t];
+        for (int t = 0; t < KS * KS; t++) wdw[(size_t)t * C + c] = w16(w1_host, (size_t)c * KS * KS + t);
+    if (i8) {
+        fcm_status st = prepare_i8(h, w1_host);
+        if (st != FCM_OK) return st;
+    }
     if (cudaMalloc(&h->wp_img, h->wp_img_bytes) != cudaSuccess ||
         cudaMemcpy(h->wp_img, img.data(), h->wp_img_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMalloc(&h->w1dw_img, wdw.size() * 2) != cudaSuccess ||
@@ -252,8 +323,12 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     if (L.stages < 1) return cudaErrorInvalidConfiguration;
     Args a;
     memset(&a, 0, sizeof(a));
-    const CUtensorMapDataType dt =
-        d.dtype == FCM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const bool i8 = d.dtype == FCM_I8;
+    if (i8 && mode == PWONLY) return cudaErrorInvalidValue;   // runs as FUSED (launch_tc_pw)
+    const CUtensorMapDataType dt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : d.dtype == FCM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t es = (cuuint64_t)fcm_dtype_bytes(d.dtype);
     CUresult cr;
     if (mode == PWONLY) {
         long long P = (long long)d.n * h->ho * h->wo;
@@ -269,8 +344,8 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
         a.num_tiles = (int)((P + kTileM - 1) / kTileM);
     } else {
         cuuint64_t gdim[4] = {(cuuint64_t)d.c, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        cuuint64_t gstride[3] = {(cuuint64_t)d.c * 2, (cuuint64_t)d.w * d.c * 2,
-                                 (cuuint64_t)d.h * d.w * d.c * 2};
+        cuuint64_t gstride[3] = {(cuuint64_t)d.c * es, (cuuint64_t)d.w * d.c * es,
+                                 (cuuint64_t)d.h * d.w * d.c * es};
         cuuint32_t box[4] = {(cuuint32_t)p.chunk_c, (cuuint32_t)p.in_cols, (cuuint32_t)p.in_rows, 1};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         cr = enc(&a.tmap, dt, 4, const_cast<void *>(in), gdim, gstride, box, estr,
@@ -291,13 +366,14 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     } else if (mode == FUSED) {
         cuuint64_t gdim[4] = {(cuuint64_t)d.k_out, (cuuint64_t)h->wo, (cuuint64_t)h->ho,
                               (cuuint64_t)d.n};
-        cuuint64_t gstride[3] = {(cuuint64_t)d.k_out * 2, (cuuint64_t)h->wo * d.k_out * 2,
-                                 (cuuint64_t)h->ho * h->wo * d.k_out * 2};
+        cuuint64_t gstride[3] = {(cuuint64_t)d.k_out * es, (cuuint64_t)h->wo * d.k_out * es,
+                                 (cuuint64_t)h->ho * h->wo * d.k_out * es};
         cuuint32_t box[4] = {64, (cuuint32_t)p.tile_w, (cuuint32_t)p.tile_h, 1};
         cuuint32_t estr[4] = {1, 1, 1, 1};
+        // staging rows of 64 elements: 128 bytes (16-bit) or 64 bytes (int8), swizzled to match
         cr = enc(&a.tmap_out, dt, 4, out, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                 i8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     a.out = out;
@@ -307,6 +383,7 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.b1 = h->b1;
     a.s2 = h->s2;
     a.b2 = h->b2;
+    a.q1 = h->q1;
     a.err = h->d_err;
     a.wait_limit_ns = kWaitLimitNs;
     a.N = d.n; a.H = d.h; a.W = d.w; a.C = h->cm; a.K = d.k_out; a.Ho = h->ho; a.Wo = h->wo;
@@ -326,7 +403,7 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.act1 = d.act1;
     a.act2 = d.act2;
     a.tmem_cols = (uint32_t)p.tmem_cols;
-    a.idesc = idesc_f16(d.dtype == FCM_BF16, kTileM, d.k_out);
+    a.idesc = idesc_f16(d.dtype == FCM_BF16, kTileM, d.k_out);   // INT8: f16 operands
     a.wp_img_bytes = (uint32_t)h->wp_img_bytes;
     a.in_stage_bytes = L.in_stage_bytes;
     a.in_stage_stride = L.in_stage_stride;
@@ -334,13 +411,17 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.off_a = L.off_a;
     a.off_out = L.off_out;
     a.out_bufs = out_bufs;
-    a.out_buf_bytes = (uint32_t)((d.k_out + 63) / 64) * kOutBlock;
+    a.out_buf_bytes = (uint32_t)((d.k_out + 63) / 64) * (uint32_t)out_block_bytes((int)es);
     a.off_in = L.off_in;
     a.off_wdw = L.off_wdw;
     a.off_sb = L.off_sb;
     a.off_bar = L.off_bar;
     const int threads = mode == PWONLY ? 32 * kFirstDwWarp : p.threads;
     const int ctas = (int)std::min<long long>(a.num_tiles, h->num_sms);
+    if (i8) {
+        if (mode == FUSED) return dispatch_ks<int8_t, FUSED>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+        return dispatch_ks<int8_t, DWONLY>(a, d.ksize, d.stride, ctas, threads, L.total, st);
+    }
     if (d.dtype == FCM_F16) {
         if (mode == FUSED) return dispatch_ks<__half, FUSED>(a, d.ksize, d.stride, ctas, threads, L.total, st);
         if (mode == DWONLY) return dispatch_ks<__half, DWONLY>(a, d.ksize, d.stride, ctas, threads, L.total, st);
@@ -359,5 +440,17 @@ cudaError_t launch_tc_dwpw(const fcm_handle *h, int mode, const void *in, void *
 }
 
 cudaError_t launch_tc_pw(const fcm_handle *h, const void *m, void *y, cudaStream_t st) {
+    if (h->d.dtype == FCM_I8) {
+        // INT8: the fused kernel over m with the identity stencil (k = 1, tap 1, scale 1,
+        // bias 0, no activation), which hands each int8 value of m to the tensor core as f16
+        fcm_handle v = *h;
+        v.d = i8_pw_desc(h);
+        v.tc = h->tc2;
+        v.s1 = h->i8_one;
+        v.b1 = h->i8_zero;
+        v.q1 = h->i8_idq;
+        v.w1dw_img = h->i8_idtap;
+        return launch_mode(&v, FUSED, m, y, st);
+    }
     return launch_mode(h, PWONLY, m, y, st);
 }

@@ -35,6 +35,7 @@ struct Args {
     const uint8_t *wp_img;     // B operand image (K rows, swizzled, K-major)
     const uint4 *wdw;          // DW taps, storage dtype, [k*k][C/8] x 8 channels
     const float *s1, *b1, *s2, *b2;
+    const float *q1;           // INT8: 1152 * sum of each channel's taps (removed from the stencil)
     unsigned *err;
     unsigned long long wait_limit_ns;
     int num_tiles;
@@ -65,7 +66,8 @@ struct Bars {
     }
 };
 constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 2 * kMaxChunks + 4 + 2) + 16;
-constexpr int kOutBlock = kTileM * 128;   // bytes of one 64-channel block of the output stage
+// bytes of one 64-channel block of the output stage (kTileM rows of 64 elements)
+constexpr int out_block_bytes(int esize) { return kTileM * 64 * esize; }
 
 // Launch dwpw_kernel<T, KS, S, MODE, DWB> (instantiated in tc_dwpw_inst_*.cu).
 template <typename T, int KS, int S, int MODE, int DWB>

@@ -25,6 +25,11 @@
 // Synchronisation is by mbarriers only; every wait is bounded (about one second) and a
 // timeout sets the device error word, raises a CTA-wide abort flag and drains in-flight
 // copies and MMAs before TMEM is released.
+//
+// T is the storage type: __half, __nv_bfloat16, or int8_t for the INT8 module (section III-B).
+// INT8 computes on the f16 paths (int8 values are exact in f16): the stencil widens its inputs
+// to f16 holding 1152 + x (I8::widen4) and removes the offset at the end, the intermediate is
+// requantized and handed to the tensor core as f16, the output is requantized to int8.
 #pragma once
 
 #include "tc_dwpw.cuh"
@@ -58,7 +63,7 @@ struct DwUnit {
     int r, oc0;       // tile row and first tile column of the unit
 };
 
-template <int S>
+template <typename T, int S>
 __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
     const int nv = a.chunk_c >> 3;
     const int v = u % nv;
@@ -68,7 +73,8 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
     d.r = rest / a.ngroups;
     d.oc0 = g * kR;
     d.cv = v * 8;
-    d.x_off = (uint32_t)((d.r * S) * a.in_cols + d.oc0 * S) * (uint32_t)a.chunk_c * 2u + (uint32_t)v * 16u;
+    d.x_off = ((uint32_t)((d.r * S) * a.in_cols + d.oc0 * S) * (uint32_t)a.chunk_c + (uint32_t)v * 8u) *
+              (uint32_t)sizeof(T);
     d.m_row0 = d.r * a.tile_w + d.oc0;
     d.nvalid = min(kR, a.tile_w - d.oc0);
     return d;
@@ -77,15 +83,18 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
 // One DW work unit.  Products of 16-bit inputs and 16-bit taps are exact; sums are fp32
 // (fma.rn.f32.{f16,bf16}).  `stage` and `wdw` are shared-memory pointers; the loads are plain
 // C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
-// which clobber memory).
+// which clobber memory).  INT8: 8-byte input vectors widened to f16 (1152 + x), f16 taps, and
+// the offset 1152 * sum(taps) of each channel (q1_s) removed at the end.
 template <typename T, int KS, int S, int MODE, int ACT, bool RT>
 __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chunk,
                                         const uint8_t *stage, const uint8_t *wdw,
                                         const uint4 (&wreg)[KS * KS], const float *s1_s,
-                                        const float *b1_s, uint32_t a_saddr, int n, int ho0,
-                                        int wo0) {
+                                        const float *b1_s, const float *q1_s, uint32_t a_saddr,
+                                        int n, int ho0, int wo0) {
+    constexpr bool kI8 = std::is_same<T, int8_t>::value;
+    using TM = typename std::conditional<kI8, __half, T>::type;   // arithmetic type
     const int c_glob = chunk * a.chunk_c + g.cv;
-    const uint32_t px_bytes = (uint32_t)a.chunk_c * 2u;
+    const uint32_t px_bytes = (uint32_t)a.chunk_c * (uint32_t)sizeof(T);
     const uint32_t row_bytes = (uint32_t)a.in_cols * px_bytes;
     const uint32_t tap_bytes = (uint32_t)a.C * 2u;   // bytes between taps of the weight image
     const uint8_t *xb = stage + g.x_off;
@@ -107,15 +116,22 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
         const uint8_t *xr = xb + (uint32_t)i * row_bytes;
 #pragma unroll
         for (int q = 0; q < (kR - 1) * S + KS; q++) {
-            const uint4 x = *reinterpret_cast<const uint4 *>(xr + (uint32_t)q * px_bytes);
+            uint4 x;
+            if constexpr (kI8) {
+                const uint2 x8 = *reinterpret_cast<const uint2 *>(xr + (uint32_t)q * px_bytes);
+                I8::widen4(x8.x, x.x, x.y);
+                I8::widen4(x8.y, x.z, x.w);
+            } else {
+                x = *reinterpret_cast<const uint4 *>(xr + (uint32_t)q * px_bytes);
+            }
 #pragma unroll
             for (int jj = 0; jj < kR; jj++) {
                 const int t = q - jj * S;
                 if (t >= 0 && t < KS) {
-                    Fma16<T>::fma2(acc[jj][0], acc[jj][1], x.x, w[t].x);
-                    Fma16<T>::fma2(acc[jj][2], acc[jj][3], x.y, w[t].y);
-                    Fma16<T>::fma2(acc[jj][4], acc[jj][5], x.z, w[t].z);
-                    Fma16<T>::fma2(acc[jj][6], acc[jj][7], x.w, w[t].w);
+                    Fma16<TM>::fma2(acc[jj][0], acc[jj][1], x.x, w[t].x);
+                    Fma16<TM>::fma2(acc[jj][2], acc[jj][3], x.y, w[t].y);
+                    Fma16<TM>::fma2(acc[jj][4], acc[jj][5], x.z, w[t].z);
+                    Fma16<TM>::fma2(acc[jj][6], acc[jj][7], x.w, w[t].w);
                 }
             }
         }
@@ -126,23 +142,46 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
     const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
     const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
+    if constexpr (kI8) {
+        const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
+        const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
+        const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int jj = 0; jj < kR; jj++)
+#pragma unroll
+            for (int c = 0; c < 8; c++) acc[jj][c] = __fsub_rn(acc[jj][c], qq[c]);
+    }
     // A-tile address of (row, c_glob): 64-channel block, 128-byte row, swizzled 16-byte chunk
     const uint32_t a_blk = a_saddr + (uint32_t)(c_glob >> 6) * (kTileM * 128u);
     const uint32_t a_chunk = (uint32_t)(c_glob >> 3) & 7u;
 #pragma unroll
     for (int jj = 0; jj < kR; jj++) {
         if (jj >= g.nvalid) break;
-        uint32_t pk[4];
+        const uint32_t m_row = (uint32_t)(g.m_row0 + jj);
+        const int ho = ho0 + g.r, wo = wo0 + g.oc0 + jj;
+        if constexpr (kI8) {
+            float v[8];
 #pragma unroll
-        for (int c = 0; c < 4; c++)
-            pk[c] = Pack2<T>::template run<ACT>(fmaf(sc[2 * c], acc[jj][2 * c], bi[2 * c]),
-                                                fmaf(sc[2 * c + 1], acc[jj][2 * c + 1], bi[2 * c + 1]));
-        if (MODE == FUSED) {
-            const uint32_t m_row = (uint32_t)(g.m_row0 + jj);
-            sts128(a_blk + m_row * 128u + ((a_chunk ^ (m_row & 7u)) << 4), pk[0], pk[1], pk[2], pk[3]);
+            for (int c = 0; c < 8; c++) v[c] = fmaf(sc[c], acc[jj][c], bi[c]);
+            if (MODE == FUSED) {
+                sts128(a_blk + m_row * 128u + ((a_chunk ^ (m_row & 7u)) << 4),
+                       I8::half2<ACT>(v[0], v[1]), I8::half2<ACT>(v[2], v[3]),
+                       I8::half2<ACT>(v[4], v[5]), I8::half2<ACT>(v[6], v[7]));
+            } else if (ho < a.Ho && wo < a.Wo) {
+                T *dst = static_cast<T *>(a.out) +
+                         (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(I8::bytes4<ACT>(v[0], v[1], v[2], v[3]),
+                                                             I8::bytes4<ACT>(v[4], v[5], v[6], v[7]));
+            }
         } else {
-            const int ho = ho0 + g.r, wo = wo0 + g.oc0 + jj;
-            if (ho < a.Ho && wo < a.Wo) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                pk[c] = Pack2<T>::template run<ACT>(fmaf(sc[2 * c], acc[jj][2 * c], bi[2 * c]),
+                                                    fmaf(sc[2 * c + 1], acc[jj][2 * c + 1], bi[2 * c + 1]));
+            if (MODE == FUSED) {
+                sts128(a_blk + m_row * 128u + ((a_chunk ^ (m_row & 7u)) << 4), pk[0], pk[1], pk[2], pk[3]);
+            } else if (ho < a.Ho && wo < a.Wo) {
                 T *dst = static_cast<T *>(a.out) +
                          (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -177,10 +216,18 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
     const int lane = threadIdx.x & 31;
     const bool has_mma = MODE != DWONLY;
     const bool has_dw = MODE != PWONLY;
+    constexpr bool kI8 = std::is_same<T, int8_t>::value;
+    static_assert(!(kI8 && MODE == PWONLY), "INT8 PW-only runs as FUSED with an identity stencil");
+    // output staging: 64-channel blocks of kTileM rows; rows of 128 bytes (16-bit, 128-byte
+    // swizzle) or 64 bytes (int8, 64-byte swizzle)
+    constexpr uint32_t kRowBytes = 64u * (uint32_t)sizeof(T);
+    constexpr uint32_t kBlockBytes = (uint32_t)kTileM * kRowBytes;
+    using TS = typename std::conditional<kI8, __half, T>::type;   // 16-bit packing (non-INT8)
 
     uint4 *wdw_s = reinterpret_cast<uint4 *>(base_g + a.off_wdw);   // filled in the prologue
     float *sb_s = reinterpret_cast<float *>(base_g + a.off_sb);
     float *s1_s = sb_s, *b1_s = sb_s + a.C, *s2_s = sb_s + 2 * a.C, *b2_s = sb_s + 2 * a.C + a.K;
+    float *q1_s = sb_s + 2 * a.C + 2 * a.K;   // INT8: 1152 * sum of each channel's taps
     const uint32_t bar_base = base_s + a.off_bar;
     Bars bars(bar_base);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base_g + a.off_bar + kBarBytes);
@@ -195,6 +242,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
         for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
             s1_s[i] = a.s1[i];
             b1_s[i] = a.b1[i];
+            if (kI8) q1_s[i] = a.q1[i];
         }
     for (int i = threadIdx.x; i < a.K; i += blockDim.x) {
         s2_s[i] = a.s2[i];
@@ -354,13 +402,30 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
         const int row = q * 32 + lane;
         const bool issuer = warp == 2 && lane == 0;
         const int nkb_out = (a.K + 63) / 64;
-        const uint32_t swz = (uint32_t)(row & 7);
-        uint32_t out_s = base_s + a.off_out, row_s = out_s + (uint32_t)row * 128;
+        const uint32_t swz = kI8 ? (uint32_t)((row >> 1) & 3) : (uint32_t)(row & 7);
+        uint32_t out_s = base_s + a.off_out, row_s = out_s + (uint32_t)row * kRowBytes;
         with_act(a.act2, [&](auto act_tag) {
             constexpr int ACT = decltype(act_tag)::value;
             // scale/bias/act on 16 accumulator columns starting at c0, rounded and written to the
             // swizzled staging row
             auto emit16 = [&](const uint32_t (&rr)[16], int c0) {
+                if constexpr (kI8) {
+                    // 16 int8 outputs = one 16-byte chunk of the 64-byte row
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; i4++) {
+                        const float4 sc = *reinterpret_cast<const float4 *>(s2_s + c0 + 4 * i4);
+                        const float4 bi = *reinterpret_cast<const float4 *>(b2_s + c0 + 4 * i4);
+                        pk[i4] = I8::bytes4<ACT>(fmaf(sc.x, __uint_as_float(rr[4 * i4]), bi.x),
+                                                 fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y),
+                                                 fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z),
+                                                 fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w));
+                    }
+                    const uint32_t blk = (uint32_t)(c0 >> 6) * kBlockBytes;
+                    const uint32_t ch = (uint32_t)((c0 & 63) >> 4);
+                    sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+                    return;
+                }
                 uint32_t pk[8];
 #pragma unroll
                 for (int i4 = 0; i4 < 4; i4++) {
@@ -370,10 +435,10 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                     const float y1 = fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), bi.y);
                     const float y2 = fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), bi.z);
                     const float y3 = fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), bi.w);
-                    pk[2 * i4] = Pack2<T>::template run<ACT>(y0, y1);
-                    pk[2 * i4 + 1] = Pack2<T>::template run<ACT>(y2, y3);
+                    pk[2 * i4] = Pack2<TS>::template run<ACT>(y0, y1);
+                    pk[2 * i4 + 1] = Pack2<TS>::template run<ACT>(y2, y3);
                 }
-                const uint32_t blk = (uint32_t)(c0 >> 6) * kOutBlock;
+                const uint32_t blk = (uint32_t)(c0 >> 6) * kBlockBytes;
                 const uint32_t ch = (uint32_t)((c0 & 63) >> 3);
                 sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
                 sts128(row_s + blk + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
@@ -393,7 +458,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                 }
                 if (named_barrier_or(1, 32 * kEpiWarps, !ok)) break;
                 out_s = base_s + a.off_out + (uint32_t)(a.out_bufs == 2 ? (lt & 1) : 0) * a.out_buf_bytes;
-                row_s = out_s + (uint32_t)row * 128;
+                row_s = out_s + (uint32_t)row * kRowBytes;
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
@@ -416,13 +481,13 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                 if (issuer) {
                     if (MODE == PWONLY) {
                         for (int kb = 0; kb < nkb_out; kb++)
-                            tma_store_2d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
+                            tma_store_2d(&a.tmap_out, out_s + (uint32_t)kb * kBlockBytes, kb * 64,
                                          t * kTileM);
                     } else {
                         int n, ho0, wo0;
                         tile_coords(a, t, n, ho0, wo0);
                         for (int kb = 0; kb < nkb_out; kb++)
-                            tma_store_4d(&a.tmap_out, out_s + (uint32_t)kb * kOutBlock, kb * 64,
+                            tma_store_4d(&a.tmap_out, out_s + (uint32_t)kb * kBlockBytes, kb * 64,
                                      wo0, ho0, n);
                     }
                     bulk_commit_group();
@@ -443,7 +508,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
             const int jm = dw_w / a.dw_per_chunk;
             const int tid = (dw_w % a.dw_per_chunk) * 32 + lane;
             const bool has_unit = tid < units;
-            const DwUnit g0 = dw_unit_geom<S>(a, has_unit ? tid : 0);
+            const DwUnit g0 = dw_unit_geom<T, S>(a, has_unit ? tid : 0);
             uint4 wreg[KS * KS];
             {
                 const uint8_t *wb = wdw_g + (uint32_t)(jm * a.chunk_c + g0.cv) * 2u;
@@ -467,7 +532,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                     const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
                     if (has_unit)
                         dw_unit<T, KS, S, MODE, ACT, true>(a, g0, jm, stage_g, wdw_g, wreg, s1_s,
-                                                           b1_s, a_s, n, ho0, wo0);
+                                                           b1_s, q1_s, a_s, n, ho0, wo0);
                     if (MODE == FUSED) fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -482,7 +547,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
             const int nthr = a.n_dw_warps * 32;
             const uint4 wnone[KS * KS] = {};
             // the thread's first unit (most plans give each thread at most one per chunk)
-            const DwUnit g0 = dw_unit_geom<S>(a, tid < units ? tid : 0);
+            const DwUnit g0 = dw_unit_geom<T, S>(a, tid < units ? tid : 0);
             with_act(a.act1, [&](auto act_tag) {
                 constexpr int ACT = decltype(act_tag)::value;
                 int lt = 0, it = 0;
@@ -505,11 +570,11 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                         const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
                         if (tid < units)
                             dw_unit<T, KS, S, MODE, ACT, false>(a, g0, j, stage_g, wdw_g, wnone, s1_s,
-                                                                b1_s, a_s, n, ho0, wo0);
+                                                                b1_s, q1_s, a_s, n, ho0, wo0);
                         for (int u = tid + nthr; u < units; u += nthr)
-                            dw_unit<T, KS, S, MODE, ACT, false>(a, dw_unit_geom<S>(a, u), j, stage_g,
-                                                                wdw_g, wnone, s1_s, b1_s, a_s, n,
-                                                                ho0, wo0);
+                            dw_unit<T, KS, S, MODE, ACT, false>(a, dw_unit_geom<T, S>(a, u), j, stage_g,
+                                                                wdw_g, wnone, s1_s, b1_s, q1_s, a_s,
+                                                                n, ho0, wo0);
                         if (MODE == FUSED) fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {

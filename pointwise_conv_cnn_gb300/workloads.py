@@ -28,7 +28,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
-DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+DTYPE_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
 BASE_SEED = 20240430
 
 
@@ -97,6 +97,11 @@ def to_storage(a: np.ndarray, dtype: str) -> np.ndarray:
         return a32.astype(np.float16)
     if dtype == "bf16":
         return f32_to_bf16_bits(a32)
+    if dtype == "i8":
+        a = np.asarray(a, dtype=np.float64)
+        if not np.array_equal(a, np.rint(a)) or a.min(initial=0) < -128 or a.max(initial=0) > 127:
+            raise ValueError("int8 storage takes integers in [-128, 127]")
+        return a.astype(np.int8)
     raise ValueError(dtype)
 
 
@@ -108,7 +113,7 @@ def to_f64(a: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def numpy_storage_dtype(dtype: str):
-    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[dtype]
+    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16, "i8": np.int8}[dtype]
 
 
 # ---------------------------------------------------------------------------- layer shapes
@@ -214,6 +219,10 @@ WORKLOADS = (
     # (ReLU6), then depthwise 3x3 s1 over the 192 channels (ReLU6)
     Workload("pwdw_f16", 64, 56, 56, 64, 192, "pwdw", 3, 1, 1, "relu6", "relu6", "f16", "normal",
              mid=192),
+    # the MobileNet DW -> PW pair in INT8 (int8 activations and weights, fp32 requantization
+    # scales); ReLU after the depthwise layer, none after the pointwise one
+    Workload("mobilenet_dwpw_i8", 64, 56, 56, 128, 128, "dw", 3, 1, 1, "relu", "none", "i8",
+             "int8"),
 )
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -246,7 +255,10 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
     """Draw a case.  kind: None -> the workload's own distribution ("uniform" or "normal");
     "integer" -> small integers (x in [-3,3], weights in [-2,2]) chosen so that every partial
     sum is exact in fp32 and the intermediate is exact in the storage format (bit-exact
-    checks); "integer1" -> the same with x and weights in [-1,1], for wide dense layers."""
+    checks); "integer1" -> the same with x and weights in [-1,1], for wide dense layers;
+    "int8" -> int8 activations and weights uniform over [-128, 127] with fp32 requantization
+    scales that put the intermediate's and the output's spread near 32 (their tails saturate)
+    and biases uniform in [-4, 4] (int8 units)."""
     seed = BASE_SEED if seed is None else seed
     kind = wl.dist if kind is None else kind
     sh = wl.shapes()
@@ -271,12 +283,23 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
             x = normal(seed, _TID["x"], cnt["x"], 1.0)
             w1 = normal(seed, _TID["w1"], cnt["w1"], (1.0 / fan1) ** 0.5)
             wp = normal(seed, _TID["wp"], cnt["wp"], (1.0 / fan2) ** 0.5)
+        elif kind == "int8":
+            x = integers(seed, _TID["x"], cnt["x"], -128, 127)
+            w1 = integers(seed, _TID["w1"], cnt["w1"], -128, 127)
+            wp = integers(seed, _TID["wp"], cnt["wp"], -128, 127)
+            sd = 73.9   # standard deviation of a uniform integer on [-128, 127]
+            rms_m = 32.0 / 2 ** 0.5 if wl.act1 in ("relu", "relu6") else 32.0
+            s1 = uniform(seed, _TID["s1"], cnt["s1"], 0.5, 1.5) * (32.0 / (sd * sd * fan1 ** 0.5))
+            s2 = uniform(seed, _TID["s2"], cnt["s2"], 0.5, 1.5) * (32.0 / (rms_m * sd * fan2 ** 0.5))
+            b1 = uniform(seed, _TID["b1"], cnt["b1"], -4.0, 4.0)
+            b2 = uniform(seed, _TID["b2"], cnt["b2"], -4.0, 4.0)
         else:
             raise ValueError(kind)
-        s1 = uniform(seed, _TID["s1"], cnt["s1"], 0.5, 1.5)
-        b1 = uniform(seed, _TID["b1"], cnt["b1"], -0.1, 0.1)
-        s2 = uniform(seed, _TID["s2"], cnt["s2"], 0.5, 1.5)
-        b2 = uniform(seed, _TID["b2"], cnt["b2"], -0.1, 0.1)
+        if kind != "int8":
+            s1 = uniform(seed, _TID["s1"], cnt["s1"], 0.5, 1.5)
+            b1 = uniform(seed, _TID["b1"], cnt["b1"], -0.1, 0.1)
+            s2 = uniform(seed, _TID["s2"], cnt["s2"], 0.5, 1.5)
+            b2 = uniform(seed, _TID["b2"], cnt["b2"], -0.1, 0.1)
     st = lambda a, name: to_storage(a.reshape(sh[name]), d)
     f32 = lambda a, name: a.reshape(sh[name]).astype(np.float32)
     return Case(wl, seed, st(x, "x"), st(w1, "w1"), st(wp, "wp"), f32(s1, "s1"), f32(b1, "b1"),
@@ -287,6 +310,8 @@ def integer_safe(wl: Workload, kind: str = "integer") -> bool:
     """True when the integer case of `wl` is exact end to end: fp32 partial sums stay below
     2^24 and the intermediate (|m| <= k*k*max|x*w| + 2, before the activation) is exactly
     representable in the storage format (2^8 for bf16, 2^11 for f16)."""
+    if wl.dtype == "i8":
+        return True   # int8 arithmetic is exact integer arithmetic at every size
     k = wl.ksize
     prod = 6 if kind == "integer" else 1
     if wl.conv1 == "pwdw":

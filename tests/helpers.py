@@ -9,14 +9,15 @@ import pointwise_conv_cnn_gb300 as fcm
 from pointwise_conv_cnn_gb300 import workloads as wk
 
 # Parity bars: fp32 max-abs error <= 1e-4 * sqrt(C) with C the 1x1 reduction length;
-# fp16/bf16 max-norm relative error <= 2e-2 (max|gpu - ref| / max|ref|).
+# fp16/bf16 max-norm relative error <= 2e-2 (max|gpu - ref| / max|ref|); INT8 exact.
 F32_ABS_PER_SQRT_C = 1e-4
 HALF_REL = 2e-2
 
 
 def torch_dtype(dtype: str):
     import torch
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+            "i8": torch.int8}[dtype]
 
 
 def to_device(arr: np.ndarray, dtype: str, device="cuda"):
@@ -40,8 +41,12 @@ def empty(shape, dtype: str, device="cuda", fill=None):
     import torch
     t = torch.empty(shape, dtype=torch_dtype(dtype), device=device)
     if fill is not None:
-        t.fill_(fill)
+        # int8 has no NaN: a value the kernels must overwrite (compared element by element)
+        t.fill_(I8_FILL if dtype == "i8" and fill != fill else fill)
     return t
+
+
+I8_FILL = -77
 
 
 def make_module(case: wk.Case, kernel: str = "auto", **desc_over) -> fcm.FusedConvModule:
@@ -66,8 +71,12 @@ def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
 
 
 def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.ndarray:
-    f = case.f64()
     wl = case.wl
+    if wl.dtype == "i8":   # int8 results, as float64 for the shared comparisons
+        return oracle.fused_i8(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2,
+                               wl.act1, wl.act2, wl.stride, wl.pad,
+                               nthreads=nthreads).astype(np.float64)
+    f = case.f64()
     if wl.conv1 == "pwdw":
         return oracle.pwdw(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
                            wl.act1, wl.act2, wl.stride, wl.pad, mid=mid, nthreads=nthreads)
@@ -76,8 +85,11 @@ def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.nda
 
 
 def oracle_conv1(case: wk.Case) -> np.ndarray:
-    f = case.f64()
     wl = case.wl
+    if wl.dtype == "i8":
+        return oracle.dw_i8(case.x, case.w1, case.s1, case.b1, wl.act1, wl.stride,
+                            wl.pad).astype(np.float64)
+    f = case.f64()
     if wl.conv1 == "pwdw":   # the 1x1 layer, over the input's extent
         return oracle.pw(f["x"], f["w1"], f["s1"], f["b1"], wl.act1)
     if wl.conv1 == "dw":
@@ -87,8 +99,11 @@ def oracle_conv1(case: wk.Case) -> np.ndarray:
 
 def oracle_pw(case: wk.Case, m: np.ndarray) -> np.ndarray:
     """The module's second convolution on an intermediate (the depthwise one for PWDW)."""
-    f = case.f64()
     wl = case.wl
+    if wl.dtype == "i8":
+        return oracle.pw_i8(np.asarray(m).astype(np.int8), case.wp, case.s2, case.b2,
+                            wl.act2).astype(np.float64)
+    f = case.f64()
     if wl.conv1 == "pwdw":
         return oracle.dw(m, f["wp"], f["s2"], f["b2"], wl.act2, wl.stride, wl.pad)
     return oracle.pw(m, f["wp"], f["s2"], f["b2"], wl.act2)
@@ -99,14 +114,14 @@ def parity_error(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str) -> float:
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.all(np.isfinite(g)), "non-finite output"
     err = float(np.abs(g - ref).max(initial=0.0))
-    if dtype == "f32":
+    if dtype in ("f32", "i8"):
         return err
     return err / max(float(np.abs(ref).max(initial=0.0)), 1e-6)
 
 
 def assert_parity(gpu_storage: np.ndarray, ref: np.ndarray, dtype: str, c_red: int) -> float:
     e = parity_error(gpu_storage, ref, dtype)
-    bar = F32_ABS_PER_SQRT_C * np.sqrt(c_red) if dtype == "f32" else HALF_REL
+    bar = {"f32": F32_ABS_PER_SQRT_C * np.sqrt(c_red), "i8": 0.0}.get(dtype, HALF_REL)
     assert e <= bar, f"parity error {e:.3e} above bar {bar:.3e}"
     return e
 

@@ -27,6 +27,12 @@ def reduced(wl: wk.Workload, n=2, hw=None) -> wk.Workload:
 
 
 def module_or_skip(case, kernel):
+    if case.wl.dtype == "i8" and kernel == "simt":
+        # INT8 has no CUDA-core kernels: the request is refused, not served by another path
+        with pytest.raises(fcm.FcmError) as e:
+            make_module(case, kernel)
+        assert e.value.status == 2
+        pytest.skip("INT8 runs on the tensor-core kernels only")
     try:
         return make_module(case, kernel)
     except fcm.FcmError as e:
@@ -182,6 +188,53 @@ def test_pwdw_edge_shapes(cuda, shape, kernel):
             assert_bitexact(got, iref, dt)
 
 
+I8_EDGE = [  # (N, H, W, C, K, k, s, p, act1, act2): the INT8 module, int8 over the full range
+    (1, 1, 1, 16, 16, 3, 1, 1, "relu", "none"),
+    (2, 13, 17, 32, 48, 3, 1, 1, "none", "relu6"),
+    (3, 9, 30, 64, 32, 5, 2, 2, "relu", "relu"),
+    (1, 7, 7, 16, 256, 7, 1, 3, "none", "none"),
+    (2, 11, 5, 48, 16, 1, 1, 0, "relu", "none"),
+    (1, 20, 131, 16, 16, 3, 1, 1, "relu", "relu"),
+    (2, 12, 14, 256, 64, 3, 2, 1, "relu6", "none"),
+    (1, 9, 40, 96, 80, 7, 2, 3, "relu", "relu6"),
+]
+
+
+@pytest.mark.parametrize("shape", I8_EDGE, ids=lambda s: "x".join(map(str, s[:8])))
+def test_int8_edge_shapes(cuda, shape):
+    """INT8 DW -> PW: bit-exact with the oracle in every mode (fused, layer by layer, the
+    depthwise layer alone, the 1x1 on the oracle's intermediate): ragged tiles, 1x1 images,
+    stride 2, k = 1, 5, 7, the widest channel counts."""
+    import torch
+    N, H, W, C, K, k, s, p, a1, a2 = shape
+    wl = wk.Workload("i8_edge", N, H, W, C, K, "dw", k, s, p, a1, a2, "i8", "int8")
+    case = wk.make_case(wl, seed=91)
+    mod = make_module(case, "tc")
+    ref = oracle_fused(case)
+    for mode in ("fused", "unfused"):
+        got, _ = run_case(case, mode, module=mod)
+        assert_bitexact(got, ref, "i8")
+    m_ref = oracle_conv1(case)
+    m_gpu, _ = run_case(case, "conv1", module=mod)
+    assert_bitexact(m_gpu, m_ref, "i8")
+    y = empty(wl.shapes()["y"], "i8", fill=float("nan"))
+    mod.run(to_device(m_ref.astype(np.int8), "i8"), y, "pw")
+    torch.cuda.synchronize()
+    mod.check()
+    assert_bitexact(to_host(y, "i8"), oracle_pw(case, m_ref), "i8")
+
+
+def test_int8_shapes_refused(cuda):
+    """INT8 requests outside the tensor-core kernels fail with FCM_ERR_UNSUPPORTED."""
+    for kw in ({"conv1": "dense", "mid": 32}, {"c": 512, "k_out": 64}):
+        wl = wk.Workload("i8_no", 1, 8, 8, kw.get("c", 32), kw.get("k_out", 32),
+                         kw.get("conv1", "dw"), 3, 1, 1, "relu", "none", "i8", "int8",
+                         mid=kw.get("mid", 0))
+        with pytest.raises(fcm.FcmError) as e:
+            make_module(wk.make_case(wl))
+        assert e.value.status == 2, kw
+
+
 def test_run_host_matches_run(cuda):
     import torch
     wl = reduced(wk.BY_NAME["mobilenet_dwpw_f16"], n=2)
@@ -195,7 +248,8 @@ def test_run_host_matches_run(cuda):
 
 
 @pytest.mark.parametrize("name,n", [("mobilenet_dwpw_f16", 5), ("b2b_dense3x3_f16", 3),
-                                    ("pwdw_f16", 9), ("tiny_dwpw_f32", 1)])
+                                    ("pwdw_f16", 9), ("tiny_dwpw_f32", 1),
+                                    ("mobilenet_dwpw_i8", 6)])
 def test_run_host_pipelined_chunks(cuda, name, n):
     """fcm_run_host splits the batch into chunks whose copies overlap the kernels (uneven
     chunks for n = 5 and 9): the result equals fcm_run on the device for every mode."""
@@ -203,11 +257,10 @@ def test_run_host_pipelined_chunks(cuda, name, n):
     wl = wk.BY_NAME[name].with_(n=n, h=min(wk.BY_NAME[name].h, 20), w=min(wk.BY_NAME[name].w, 20))
     case = wk.make_case(wl)
     mod = make_module(case)
-    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wl.dtype]
     x_h = to_device(case.x, wl.dtype, "cpu").pin_memory()
     for mode, out_key in (("fused", "y"), ("conv1", "m"), ("unfused", "y")):
         want, _ = run_case(case, mode, module=mod)
-        got = torch.full(wl.shapes()[out_key], float("nan"), dtype=tdt).pin_memory()
+        got = empty(wl.shapes()[out_key], wl.dtype, "cpu", fill=float("nan")).pin_memory()
         mod.run_host(x_h, got, mode)
         assert np.array_equal(to_host(got, wl.dtype), want), mode
 

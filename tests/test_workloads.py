@@ -48,9 +48,15 @@ def test_case_shapes_and_storage(wl):
     sh = small.shapes()
     assert case.x.shape == sh["x"] and case.w1.shape == sh["w1"] and case.wp.shape == sh["wp"]
     assert case.x.dtype == wk.numpy_storage_dtype(wl.dtype)
+    f = case.f64()
+    if wl.dist == "int8":
+        # int8 over the full range; requantization scales positive, biases within +-4
+        assert case.x.min() == -128 and case.x.max() == 127 and case.wp.min() == -128
+        assert case.s1.dtype == np.float32 and case.s1.min() > 0 and case.s2.min() > 0
+        assert np.abs(case.b1).max() <= 4.0 and np.abs(case.b2).max() <= 4.0
+        return
     assert case.s1.dtype == np.float32 and case.s1.min() >= 0.5 and case.s1.max() <= 1.5
     assert np.abs(case.b2).max() <= 0.1
-    f = case.f64()
     if wl.dist == "normal":
         fan1, fan2 = wl.fan_in()
         assert abs(f["w1"].std() - fan1 ** -0.5) < 0.25 * fan1 ** -0.5
