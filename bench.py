@@ -33,6 +33,13 @@ L2_BYTES = 129 * 1024 * 1024
 DEFAULT_WORKLOAD = "mobilenet_dwpw_f16"
 DATA = ("synthetic: seeded splitmix64 streams; activations N(0,1), weights N(0,1/fan_in), "
         "scale U[0.5,1.5], bias U[-0.1,0.1] (uniform[-1,1] for the fp32 layer)")
+DATA_I8 = ("synthetic: seeded splitmix64 streams; int8 activations and weights uniform on "
+           "[-128,127], fp32 requantization scales U[0.5,1.5] x 32/(spread of the accumulator), "
+           "biases U[-4,4]")
+
+
+def data_of(wl) -> str:
+    return DATA_I8 if wl.dtype == "i8" else DATA
 
 
 def parse():
@@ -326,7 +333,7 @@ def run_ours(args):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(region_ms / steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"i8": "int8"}.get(wl.dtype, wl.dtype),
-        "data": DATA,
+        "data": data_of(wl),
         "config": {"workload": wl.name, "n": wl.n, "h": wl.h, "w": wl.w, "c": wl.c,
                    "k_out": wl.k_out, "conv1": wl.conv1, "ksize": wl.ksize, "stride": wl.stride,
                    "pad": wl.pad, "act1": wl.act1, "act2": wl.act2, "mode": args.mode,
@@ -417,7 +424,7 @@ def run_reference(args):
            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
-           "dtype": "int8" if wl.dtype == "i8" else "f64", "data": DATA,
+           "dtype": "int8" if wl.dtype == "i8" else "f64", "data": data_of(wl),
            "config": {"workload": wl.name, "n": wl.n, "h": wl.h, "w": wl.w, "c": wl.c,
                       "k_out": wl.k_out, "images_per_step": n_img},
            "images_per_s": round(n_img / dt, 4),
