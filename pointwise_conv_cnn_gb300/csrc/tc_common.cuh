@@ -238,7 +238,7 @@ struct I8 {
     static constexpr float kBias = 1152.0f;
     // Four int8 lanes -> two f16x2 holding 1152 + x: the byte x ^ 0x80 = x + 128 (0..255) is
     // placed in the low mantissa bits of 0x6400.  The stencil sums (1152 + x) * w over its taps
-    // and subtracts 1152 * (sum of the channel's taps) at the end; every step is exact.
+    // starting from -1152 * (sum of the channel's taps); every step is exact.
     static __device__ __forceinline__ void widen4(uint32_t x4, uint32_t &lo, uint32_t &hi) {
         const uint32_t u = x4 ^ 0x80808080u;
         lo = __byte_perm(u, 0x64646464u, 0x4140);
@@ -256,12 +256,21 @@ struct I8 {
         return __fadd_rn(fminf(fmaxf(v, lo), hi), kRound);
     }
     // Two requantized values as f16x2 (`lo` in the low half): the A operand of the 1x1 GEMM.
+    // With ReLU/ReLU6 the lower clamp is the conversion's own .relu: any negative v rounds to
+    // a value <= 0 (rounding is monotonic), which .relu turns into 0.
     template <int ACT>
     static __device__ __forceinline__ uint32_t half2(float lo, float hi) {
-        const float rl = __fsub_rn(biased<ACT>(lo), kRound);
-        const float rh = __fsub_rn(biased<ACT>(hi), kRound);
         uint32_t r;
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(rh), "f"(rl));
+        if (ACT == 0) {
+            const float rl = __fsub_rn(biased<ACT>(lo), kRound);
+            const float rh = __fsub_rn(biased<ACT>(hi), kRound);
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(rh), "f"(rl));
+        } else {
+            const float top = ACT == 2 ? 6.0f : 127.0f;
+            const float rl = __fsub_rn(__fadd_rn(fminf(lo, top), kRound), kRound);
+            const float rh = __fsub_rn(__fadd_rn(fminf(hi, top), kRound), kRound);
+            asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(rh), "f"(rl));
+        }
         return r;
     }
     // Four requantized values packed as int8 lanes (a in the lowest byte).

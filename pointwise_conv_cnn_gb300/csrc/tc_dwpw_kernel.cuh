@@ -28,7 +28,7 @@
 //
 // T is the storage type: __half, __nv_bfloat16, or int8_t for the INT8 module (section III-B).
 // INT8 computes on the f16 paths (int8 values are exact in f16): the stencil widens its inputs
-// to f16 holding 1152 + x (I8::widen4) and removes the offset at the end, the intermediate is
+// to f16 holding 1152 + x (I8::widen4) and starts its sums at minus the offset, the intermediate is
 // requantized and handed to the tensor core as f16, the output is requantized to int8.
 #pragma once
 
@@ -84,7 +84,7 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
 // (fma.rn.f32.{f16,bf16}).  `stage` and `wdw` are shared-memory pointers; the loads are plain
 // C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
 // which clobber memory).  INT8: 8-byte input vectors widened to f16 (1152 + x), f16 taps, and
-// the offset 1152 * sum(taps) of each channel (q1_s) removed at the end.
+// the sums started at -1152 * sum(taps) of each channel (q1_s), which the offsets cancel.
 template <typename T, int KS, int S, int MODE, int ACT, bool RT>
 __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chunk,
                                         const uint8_t *stage, const uint8_t *wdw,
@@ -100,11 +100,22 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     const uint8_t *xb = stage + g.x_off;
     const uint8_t *wb = wdw + (uint32_t)c_glob * 2u;
 
+    // INT8: the sums start at -1152 * sum(taps), the offset the widened inputs carry
     float acc[kR][8];
+    if constexpr (kI8) {
+        const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
+        const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
+        const float qq[8] = {-q0.x, -q0.y, -q0.z, -q0.w, -q1.x, -q1.y, -q1.z, -q1.w};
 #pragma unroll
-    for (int jj = 0; jj < kR; jj++)
+        for (int jj = 0; jj < kR; jj++)
 #pragma unroll
-        for (int c = 0; c < 8; c++) acc[jj][c] = 0.0f;
+            for (int c = 0; c < 8; c++) acc[jj][c] = qq[c];
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < kR; jj++)
+#pragma unroll
+            for (int c = 0; c < 8; c++) acc[jj][c] = 0.0f;
+    }
 
 #pragma unroll
     for (int i = 0; i < KS; i++) {
@@ -142,15 +153,6 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
     const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
     const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
-    if constexpr (kI8) {
-        const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
-        const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
-        const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int jj = 0; jj < kR; jj++)
-#pragma unroll
-            for (int c = 0; c < 8; c++) acc[jj][c] = __fsub_rn(acc[jj][c], qq[c]);
-    }
     // A-tile address of (row, c_glob): 64-channel block, 128-byte row, swizzled 16-byte chunk
     const uint32_t a_blk = a_saddr + (uint32_t)(c_glob >> 6) * (kTileM * 128u);
     const uint32_t a_chunk = (uint32_t)(c_glob >> 3) & 7u;
