@@ -117,3 +117,25 @@ def test_pwdw_plan_models_match_literal():
     assert info["gma_fused_model"] == fused * wl.n * e
     # the intermediate (N x H x W x Cm) is what fusion keeps out of HBM
     assert info["bytes_unfused_min"] - info["bytes_fused_min"] == 2 * wl.n * H * W * Cm * e
+
+
+def test_int8_plans_and_refusals():
+    """INT8 (FCM_I8): the depthwise module plans on the tensor-core kernels with 1-byte
+    activations and weights (scales and biases stay fp32); requests without an INT8 kernel are
+    refused with FCM_ERR_UNSUPPORTED, never served by another path."""
+    f16 = wk.BY_NAME["mobilenet_dwpw_f16"]
+    i8 = wk.BY_NAME["mobilenet_dwpw_i8"]
+    pi = fcm.fcm_plan_desc(fcm.desc_from_workload(i8))
+    pf = fcm.fcm_plan_desc(fcm.desc_from_workload(f16))
+    assert pi["kernel"] == 2
+    sb = 4 * (2 * i8.c + 2 * i8.k_out)
+    assert pi["bytes_fused_min"] - sb == (pf["bytes_fused_min"] - sb) // 2
+    refused = [i8.with_(conv1="dense", mid=128), i8.with_(conv1="pwdw", mid=128, k_out=128),
+               i8.with_(c=512, k_out=64)]
+    for wl in refused:
+        with pytest.raises(fcm.FcmError) as e:
+            fcm.fcm_plan_desc(fcm.desc_from_workload(wl))
+        assert e.value.status == 2, wl
+    with pytest.raises(fcm.FcmError) as e:
+        fcm.fcm_plan_desc(fcm.desc_from_workload(i8, kernel="simt"))
+    assert e.value.status == 2

@@ -40,16 +40,17 @@ def _run_both(wl, kernel):
 
 
 @pytest.mark.parametrize("name,kernel", [("mobilenet_dwpw_f16", "auto"), ("stride2_dwpw_bf16", "auto"),
-                                         ("mobilenet_dwpw_f16", "simt"), ("tiny_dwpw_f32", "auto")])
+                                         ("mobilenet_dwpw_f16", "simt"), ("tiny_dwpw_f32", "auto"),
+                                         ("mobilenet_dwpw_i8", "auto")])
 def test_static_scratch_matches_allocating_path(cuda, name, kernel):
     wl = wk.BY_NAME[name]
     wl = wl.with_(n=min(wl.n, 2))
     case, ref, outs = _run_both(wl, kernel)
-    bar = 1e-4 * np.sqrt(wl.cm) if wl.dtype == "f32" else 2e-2
+    bar = {"f32": 1e-4 * np.sqrt(wl.cm), "i8": 0.0}.get(wl.dtype, 2e-2)
     f_ref = wk.to_f64(ref, wl.dtype)
     for got in outs:
         err = float(np.abs(wk.to_f64(got, wl.dtype) - f_ref).max())
-        if wl.dtype != "f32":
+        if wl.dtype not in ("f32", "i8"):
             err /= max(float(np.abs(f_ref).max()), 1e-6)
         assert err <= bar, (name, kernel, err)
     # and both paths against the oracle
