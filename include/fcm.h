@@ -184,6 +184,14 @@ FCM_API fcm_status fcm_run_unfused_static(fcm_handle *h, const void *in, void *o
  * own check failed, FCM_OK otherwise. */
 FCM_API fcm_status fcm_check(fcm_handle *h, void *stream);
 
+/* Self-test of the kernels' failure detection on the current device: one kernel waits, through
+ * the bounded wait every tensor-core kernel uses, on an mbarrier phase that nothing completes.
+ * After `limit_ns` (in (0, 10 s]) the wait gives up, sets a device error word and the kernel
+ * returns, leaving the context usable.  Returns FCM_ERR_TIMEOUT when that happened as designed
+ * (the expected result), FCM_ERR_DEVICE_FAULT if the wait did not report it, FCM_ERR_CUDA on a
+ * CUDA failure, FCM_ERR_INVALID_ARG for a limit out of range.  Synchronizes the device. */
+FCM_API fcm_status fcm_selftest_wait_timeout(unsigned long long limit_ns);
+
 /* The plan of an existing handle. */
 FCM_API fcm_status fcm_plan(const fcm_handle *h, fcm_plan_info *info);
 

@@ -21,7 +21,7 @@ __all__ = [
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_model_pwdw_gma",
     "fcm_model_pwpw_gma", "fcm_fuse_plan", "FcmLayer", "FcmLayerPlan", "LAYER_KINDS", "MODULES",
     "EXPORTED_SYMBOLS",
-    "fcm_run_unfused_static",
+    "fcm_run_unfused_static", "fcm_selftest_wait_timeout",
     "DTYPES", "ACTS", "MODES",
 ]
 
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_run_unfused_static",
+    "fcm_selftest_wait_timeout",
     "fcm_model_pwdw_gma", "fcm_model_pwpw_gma", "fcm_fuse_plan",
 )
 
@@ -116,11 +117,12 @@ def load_library(path: str | None = None):
         lib.fcm_run_host.argtypes = [vp, i, vp, vp, vp]
         lib.fcm_run_unfused_static.argtypes = [vp, vp, vp, vp]
         lib.fcm_check.argtypes = [vp, vp]
+        lib.fcm_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong]
         lib.fcm_plan.argtypes = [vp, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_plan_desc.argtypes = [ctypes.POINTER(FcmDesc), i, i, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_tensor_bytes.argtypes = [ctypes.POINTER(FcmDesc)] + [ctypes.POINTER(ctypes.c_size_t)] * 3
         for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_run_unfused_static", "fcm_check", "fcm_plan",
-                  "fcm_plan_desc", "fcm_tensor_bytes"):
+                  "fcm_plan_desc", "fcm_tensor_bytes", "fcm_selftest_wait_timeout"):
             getattr(lib, f).restype = i
         lib.fcm_destroy.argtypes = [vp]
         lib.fcm_destroy.restype = None
@@ -190,6 +192,12 @@ def fcm_run_unfused_static(handle: int, inp: int, out: int, stream: int = 0) -> 
 
 def fcm_check(handle: int, stream: int = 0) -> None:
     _check(load_library().fcm_check(handle, stream))
+
+
+def fcm_selftest_wait_timeout(limit_ns: int) -> None:
+    """Make one bounded device wait run out (see include/fcm.h); raises FcmError with status
+    FCM_ERR_TIMEOUT (6) when the failure detection works as designed."""
+    _check(load_library().fcm_selftest_wait_timeout(int(limit_ns)))
 
 
 def fcm_plan(handle: int) -> dict:

@@ -116,3 +116,11 @@ def test_product_path_never_touches_the_oracle():
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                          cwd=os.path.dirname(pkg))
     assert out.returncode == 0 and "raised" in out.stdout, out.stderr
+
+
+def test_selftest_limit_checked_on_the_host(lib):
+    """The wait self-test validates its limit before touching a device."""
+    for bad in (0, 10_000_000_001):
+        with pytest.raises(fcm.FcmError) as e:
+            fcm.fcm_selftest_wait_timeout(bad)
+        assert e.value.status == 1

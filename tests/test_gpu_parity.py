@@ -314,3 +314,18 @@ def test_full_size_sampled(cuda, wl):
                       case.b1, case.s2, case.b2)
         assert_parity(got[i:i + 1], oracle_fused(sub), wl.dtype, wl.cm)
     assert np.all(np.isfinite(wk.to_f64(got, wl.dtype)))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda):
+    """Failure detection: a kernel's bounded wait on an mbarrier phase that nothing completes
+    gives up after its limit and reports FCM_ERR_TIMEOUT; the CUDA context stays usable."""
+    import time
+    t0 = time.monotonic()
+    with pytest.raises(fcm.FcmError) as e:
+        fcm.fcm_selftest_wait_timeout(2_000_000)   # 2 ms
+    assert e.value.status == 6, e.value
+    assert time.monotonic() - t0 < 5.0
+    wl = reduced(wk.BY_NAME["mobilenet_dwpw_i8"], n=1, hw=14)
+    case = wk.make_case(wl)
+    got, _ = run_case(case, "fused")
+    assert_bitexact(got, oracle_fused(case), "i8")
