@@ -154,14 +154,17 @@ def torch_dtype(torch, dtype):
             "i8": torch.int8}[dtype]
 
 
-def oracle_step(oracle, wk, wl, case):
-    """One evaluation of the oracle's single-pass module on `case` (fp64, or the INT8 one)."""
+def oracle_step(oracle, wk, wl, case, nthreads: int):
+    """One evaluation of the oracle's single-pass module on `case` (fp64, or the INT8 one) with
+    `nthreads` OpenMP threads (the oracle's thread count is sticky, so every call sets it)."""
     if wl.dtype == "i8":
         return lambda: oracle.fused_i8(case.x, case.w1, case.s1, case.b1, case.wp, case.s2,
-                                       case.b2, wl.act1, wl.act2, wl.stride, wl.pad)
+                                       case.b2, wl.act1, wl.act2, wl.stride, wl.pad,
+                                       nthreads=nthreads)
     f = case.f64()
     return lambda: oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
-                                wl.act1, wl.act2, wl.stride, wl.pad, conv1=wl.conv1)
+                                wl.act1, wl.act2, wl.stride, wl.pad, conv1=wl.conv1,
+                                nthreads=nthreads)
 
 
 def storage_tensor(torch, arr, dtype):
@@ -220,9 +223,21 @@ def time_ours(torch, fcm, wk, wl, mode, kernel, steps, warmup, device, dist=None
     res = {"region_ms": region_ms, "ms_per_step": region_ms / steps,
            "kernel_ms_mean": statistics.fmean(launch_ms),
            "kernel_ms_median": statistics.median(launch_ms),
+           "kernel_ms_p10": percentile(launch_ms, 10), "kernel_ms_p90": percentile(launch_ms, 90),
            "nsets": nsets, "set_bytes": set_bytes, "plan": mod.plan, "clocks": clocks,
            "launches": steps * launches_per_step, "case": case, "module": mod}
     return res
+
+
+def percentile(values, q: float) -> float:
+    """q-th percentile, linear between the closest ranks."""
+    v = sorted(values)
+    if not v:
+        return float("nan")
+    pos = (len(v) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
 def time_e2e(torch, mod, case, wl, mode, steps, device):
@@ -255,19 +270,26 @@ def cpu_baseline(wk, wl, seconds: float) -> dict:
 
     def timed(n_img, reps):
         sub = wl.with_(n=n_img)
-        run = oracle_step(oracle, wk, sub, wk.make_case(sub))
+        run = oracle_step(oracle, wk, sub, wk.make_case(sub), threads)
         t = time.perf_counter()
         for _ in range(reps):
             run()
         return time.perf_counter() - t
 
     t1 = timed(1, 1)
+    # one image on one core, for the single-threaded figure
+    sub1 = wl.with_(n=1)
+    run1 = oracle_step(oracle, wk, sub1, wk.make_case(sub1), 1)
+    ts = time.perf_counter()
+    run1()
+    t_single = time.perf_counter() - ts
     n_img = int(max(1, min(wl.n, seconds / max(t1, 1e-6))))
     reps = max(1, int(seconds / max(t1 * n_img, 1e-6)))
     t = timed(n_img, reps)
     ips = n_img * reps / t
     return {"value": round(ips * per_image_bytes / 1e9, 6), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "images_per_s": round(ips, 4),
+            "single_thread_images_per_s": round(1.0 / t_single, 4),
             "sample": f"{n_img} of {wl.n} images of {wl.name} x {reps} passes, "
                       f"{'INT8 oracle_fused_i8' if wl.dtype == 'i8' else 'fp64 oracle_fused'}, "
                       f"{threads} OpenMP threads, {t:.2f} s"}
@@ -349,6 +371,9 @@ def run_ours(args):
                      "traffic": ncu_traffic(wl.name, args.mode),
                      "bytes_per_launch": mb["fused"],
                      "kernel_us_mean": round(res["kernel_ms_mean"] * 1e3, 3),
+                     "kernel_us_median": round(res["kernel_ms_median"] * 1e3, 3),
+                     "kernel_us_p10": round(res["kernel_ms_p10"] * 1e3, 3),
+                     "kernel_us_p90": round(res["kernel_ms_p90"] * 1e3, 3),
                      "peak_source": peaks["source"]},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": hb,
                 "d2h_bytes_per_step": db, "ms_per_step": round(e2e_ms, 4)},
@@ -388,6 +413,9 @@ def report_all(torch, fcm, wk, device):
                              "chosen": {1: "simt", 2: "tcgen05"}[r["plan"]["kernel"]],
                              "us_per_step": round(r["ms_per_step"] * 1e3, 3),
                              "kernel_us": round(ks * 1e6, 3),
+                             "kernel_us_median": round(r["kernel_ms_median"] * 1e3, 3),
+                             "kernel_us_p10_p90": [round(r["kernel_ms_p10"] * 1e3, 3),
+                                                   round(r["kernel_ms_p90"] * 1e3, 3)],
                              "images_per_s": round(wl.n / (r["ms_per_step"] / 1e3), 1),
                              "algo_gbs": round(mb["fused"] / ks / 1e9, 1),
                              "frac_hbm": round(mb["fused"] / ks / 1e9 / peaks["hbm_gbs"], 4),
@@ -410,7 +438,7 @@ def run_reference(args):
     threads = oracle.max_threads()
     n_img = 1 if wl.n > 1 else wl.n
     sub = wl.with_(n=n_img)
-    step = oracle_step(oracle, wk, sub, wk.make_case(sub))
+    step = oracle_step(oracle, wk, sub, wk.make_case(sub), threads)
 
     for _ in range(args.warmup):
         step()
