@@ -117,3 +117,18 @@ def test_chain_validation():
     assert e.value.status == 1
     with pytest.raises(fcm.FcmError):
         fcm.fcm_fuse_plan([dict(kind="dw", h=8, w=8, c=16, k_out=8, ksize=3, stride=1, pad=1)])
+
+
+def test_int8_bit_width_changes_the_fusion_decision():
+    """Section V-B: changing the bit width changes the tiles, so FusePlanner chooses differently
+    (most INT8 FCMs are fusions not feasible in FP32).  The PWPW pair above with 64 KiB of L1:
+    FP32 holds 16384 elements, fewer than the FCM's five tiles need (21504), so the layers stay
+    apart; INT8 holds 65536 and the pair is fused.  The literal model agrees in both cases."""
+    layers = [dict(kind="pw", h=4, w=4, c=32, k_out=256), dict(kind="pw", h=4, w=4, c=256, k_out=32)]
+    l1 = 64 * 1024
+    for elem_bytes, fused in ((4, 0), (1, 1)):
+        plans, total = fcm.fcm_fuse_plan(layers, 1, 1, l1, elem_bytes)
+        ref, ref_total = pm.plan_chain(layers, 1, 1, l1 // elem_bytes)
+        assert plans[0]["fuse_with_next"] == fused == ref[0]["fuse_with_next"], elem_bytes
+        assert total == ref_total
+    assert fcm.fcm_fuse_plan(layers, 1, 1, l1, 1)[1] == 17408
