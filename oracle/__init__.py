@@ -8,7 +8,7 @@ from it.
 The arithmetic lives in ``fcm_oracle.c`` (plain loops, fp64).  This module only builds that
 file with gcc, loads it with ctypes and marshals numpy arrays.  Inputs of any float dtype are
 upcast to float64 exactly before the call; outputs are float64.  The INT8 functions
-(``dw_i8``, ``pw_i8``, ``fused_i8``) take int8 activations and weights and fp32 scales and
+(``dw_i8``, ``pw_i8``, ``fused_i8``, ``dense_i8``, ``fused_dense_i8``) take int8 activations and weights and fp32 scales and
 biases, and return int8 (section III-B's INT8 FCMs).
 
 Definitions followed (see the C file for the full list): "Fusing Depthwise and Pointwise
@@ -68,9 +68,11 @@ def bind(path: str):
     lib.oracle_pw_i8.argtypes = [i] * 5 + [bp, bp, fp, fp, i, bp, i]
     lib.oracle_fused_i8.argtypes = [i] * 8 + [bp, bp, fp, fp, i, bp, fp, fp, i, bp, i]
     lib.oracle_requant_i8.argtypes = [ctypes.c_longlong, ctypes.c_float, ctypes.c_float, i]
+    lib.oracle_dense_i8.argtypes = [i] * 8 + [bp, bp, fp, fp, i, bp, i]
+    lib.oracle_fused_dense_i8.argtypes = [i] * 9 + [bp, bp, fp, fp, i, bp, fp, fp, i, bp, i]
     for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused, lib.oracle_pwdw,
               lib.oracle_max_threads, lib.oracle_dw_i8, lib.oracle_pw_i8, lib.oracle_fused_i8,
-              lib.oracle_requant_i8):
+              lib.oracle_requant_i8, lib.oracle_dense_i8, lib.oracle_fused_dense_i8):
         f.restype = ctypes.c_int
     return lib
 
@@ -268,6 +270,42 @@ def fused_i8(x, wd, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1, pad=
                                     _p8(y), nthreads)
     if rc != 0:
         raise ValueError("oracle_fused_i8: invalid shape")
+    return y
+
+
+def dense_i8(x, w1, s1, b1, act1="none", stride=1, pad=0, nthreads=0, lib=None) -> np.ndarray:
+    """INT8 dense conv: x [N,H,W,C] int8, w1 [Cm,k,k,C] int8, s1/b1 fp32 -> m int8."""
+    x, w1 = _i8(x), _i8(w1)
+    s1, b1 = _f32(s1), _f32(b1)
+    N, H, W, C = x.shape
+    Cm, k = w1.shape[0], w1.shape[1]
+    assert w1.shape == (Cm, k, k, C) and s1.shape == (Cm,) and b1.shape == (Cm,)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    m = np.empty((N, Ho, Wo, Cm), np.int8)
+    rc = _load(lib).oracle_dense_i8(N, H, W, C, Cm, k, stride, pad, _p8(x), _p8(w1), _p32(s1),
+                                    _p32(b1), ACT[act1], _p8(m), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_dense_i8: invalid shape")
+    return m
+
+
+def fused_dense_i8(x, w1, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1, pad=0,
+                   nthreads=0, lib=None) -> np.ndarray:
+    """INT8 dense k x k -> 1x1 module in one pass (PWPW for k = 1): x [N,H,W,C], w1 [Cm,k,k,C],
+    wp [K,Cm] int8; s1/b1 [Cm], s2/b2 [K] fp32 -> y [N,Ho,Wo,K] int8."""
+    x, w1, wp = _i8(x), _i8(w1), _i8(wp)
+    s1, b1, s2, b2 = map(_f32, (s1, b1, s2, b2))
+    N, H, W, C = x.shape
+    Cm, k = w1.shape[0], w1.shape[1]
+    K = wp.shape[0]
+    assert w1.shape == (Cm, k, k, C) and wp.shape == (K, Cm)
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    y = np.empty((N, Ho, Wo, K), np.int8)
+    rc = _load(lib).oracle_fused_dense_i8(N, H, W, C, Cm, K, k, stride, pad, _p8(x), _p8(w1),
+                                          _p32(s1), _p32(b1), ACT[act1], _p8(wp), _p32(s2),
+                                          _p32(b2), ACT[act2], _p8(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_fused_dense_i8: invalid shape")
     return y
 
 

@@ -421,3 +421,84 @@ int oracle_fused_i8(int N, int H, int W, int C, int K, int k, int s, int p,
     }
     return failed ? -1 : 0;
 }
+
+/* INT8 dense k x k convolution C -> Cm + requantization (the back-to-back CONV1; with k = 1
+ * the first layer of the PWPW module).  w1 [Cm][k][k][C]. */
+int oracle_dense_i8(int N, int H, int W, int C, int Cm, int k, int s, int p,
+                    const int8_t *x, const int8_t *w1, const float *s1, const float *b1, int act1,
+                    int8_t *m, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Cm < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int j = 0; j < Cm; j++) {
+                    int64_t t = 0;
+                    for (int r = 0; r < k; r++) {
+                        int hi = ho * s - p + r;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int u = 0; u < k; u++) {
+                            int wi = wo * s - p + u;
+                            if (wi < 0 || wi >= W) continue;
+                            for (int c = 0; c < C; c++)
+                                t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *
+                                     (int64_t)w1[IDX4(j, r, u, c, k, k, C)];
+                        }
+                    }
+                    m[IDX4(n, ho, wo, j, Ho, Wo, Cm)] = requant_i8(t, s1[j], b1[j], act1);
+                }
+    return 0;
+}
+
+/* The INT8 dense k x k -> 1x1 module (PWPW when k = 1) as its own single pass: one output
+ * pixel at a time, its int8 intermediate vector over all Cm channels, then the 1x1
+ * convolution of it.  It does not call oracle_dense_i8/oracle_pw_i8. */
+int oracle_fused_dense_i8(int N, int H, int W, int C, int Cm, int K, int k, int s, int p,
+                          const int8_t *x, const int8_t *w1, const float *s1, const float *b1,
+                          int act1, const int8_t *wp, const float *s2, const float *b2, int act2,
+                          int8_t *y, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Cm < 1 || K < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        int8_t *mid = (int8_t *)malloc((size_t)Cm);
+        if (!mid) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for collapse(2) schedule(static)
+        for (int n = 0; n < N; n++)
+            for (int ho = 0; ho < Ho; ho++) {
+                if (!mid) continue;
+                for (int wo = 0; wo < Wo; wo++) {
+                    for (int j = 0; j < Cm; j++) {
+                        int64_t t = 0;
+                        for (int r = 0; r < k; r++) {
+                            int hi = ho * s - p + r;
+                            if (hi < 0 || hi >= H) continue;
+                            for (int u = 0; u < k; u++) {
+                                int wi = wo * s - p + u;
+                                if (wi < 0 || wi >= W) continue;
+                                for (int c = 0; c < C; c++)
+                                    t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *
+                                         (int64_t)w1[IDX4(j, r, u, c, k, k, C)];
+                            }
+                        }
+                        mid[j] = requant_i8(t, s1[j], b1[j], act1);
+                    }
+                    for (int kk = 0; kk < K; kk++) {
+                        int64_t t = 0;
+                        for (int j = 0; j < Cm; j++)
+                            t += (int64_t)mid[j] * (int64_t)wp[(size_t)kk * Cm + j];
+                        y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], b2[kk], act2);
+                    }
+                }
+            }
+        free(mid);
+    }
+    return failed ? -1 : 0;
+}

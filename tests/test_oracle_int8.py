@@ -180,8 +180,72 @@ def pin_i8_fused_composition(lib=None):
     return True
 
 
+def dense_np(x, w1, s1, b1, act, stride, pad):
+    """Dense k x k conv in int64 (w1 [Cm,k,k,C]) from sliding windows, then requantization."""
+    N, H, W, C = x.shape
+    Cm, k = w1.shape[0], w1.shape[1]
+    Ho, Wo = (H + 2 * pad - k) // stride + 1, (W + 2 * pad - k) // stride + 1
+    xp = np.zeros((N, H + 2 * pad, W + 2 * pad, C), np.int64)
+    xp[:, pad:pad + H, pad:pad + W, :] = x
+    acc = np.zeros((N, Ho, Wo, Cm), np.int64)
+    for i in range(k):
+        for j in range(k):
+            win = xp[:, i:i + (Ho - 1) * stride + 1:stride, j:j + (Wo - 1) * stride + 1:stride, :]
+            acc += win @ w1[:, i, j, :].astype(np.int64).T
+    q, exact = requant_np(acc, np.broadcast_to(s1, acc.shape), np.broadcast_to(b1, acc.shape), act)
+    assert exact.all()
+    return q
+
+
+DENSE_CASES = [  # (N, H, W, C, Cm, K, k, stride, pad, act1, act2)
+    (1, 5, 6, 3, 4, 2, 1, 1, 0, "relu", "none"),
+    (2, 4, 7, 8, 5, 3, 1, 1, 0, "none", "relu6"),
+    (1, 6, 5, 3, 4, 2, 3, 1, 1, "relu", "relu"),
+    (1, 7, 7, 2, 3, 4, 3, 2, 1, "none", "none"),
+]
+
+
+def draw_dense(r, N, H, W, C, Cm, K, k):
+    x = r.integers(-128, 128, (N, H, W, C)).astype(np.int8)
+    w1 = r.integers(-128, 128, (Cm, k, k, C)).astype(np.int8)
+    wp = r.integers(-128, 128, (K, Cm)).astype(np.int8)
+    s1 = (r.uniform(0.5, 1.5, Cm) * 32 / (5461 * k * np.sqrt(C))).astype(np.float32)
+    b1 = r.uniform(-4, 4, Cm).astype(np.float32)
+    s2 = (r.uniform(0.5, 1.5, K) * 32 / (74 * 23 * np.sqrt(Cm))).astype(np.float32)
+    b2 = r.uniform(-4, 4, K).astype(np.float32)
+    return x, w1, wp, s1, b1, s2, b2
+
+
+def pin_i8_dense_numpy(lib=None):
+    """The dense layer and the single-pass dense -> 1x1 module against int64 numpy."""
+    r = rng(23)
+    for (N, H, W, C, Cm, K, k, st, p, a1, a2) in DENSE_CASES:
+        x, w1, wp, s1, b1, s2, b2 = draw_dense(r, N, H, W, C, Cm, K, k)
+        m = dense_np(x, w1, s1, b1, a1, st, p)
+        if not np.array_equal(oracle.dense_i8(x, w1, s1, b1, a1, st, p, lib=lib), m):
+            return False
+        got = oracle.fused_dense_i8(x, w1, s1, b1, wp, s2, b2, a1, a2, st, p, lib=lib)
+        if not np.array_equal(got, pw_np(m, wp, s2, b2, a2)):
+            return False
+    return True
+
+
+def pin_i8_pwpw_composition(lib=None):
+    """k = 1: the dense module is two 1x1 layers, pw_i8(pw_i8(x)) (the oracle's own paths)."""
+    r = rng(29)
+    for (N, H, W, C, Cm, K, k, st, p, a1, a2) in DENSE_CASES[:2]:
+        x, w1, wp, s1, b1, s2, b2 = draw_dense(r, N, H, W, C, Cm, K, k)
+        m = oracle.pw_i8(x, w1.reshape(Cm, C), s1, b1, a1, lib=lib)
+        want = oracle.pw_i8(m, wp, s2, b2, a2, lib=lib)
+        if not np.array_equal(oracle.fused_dense_i8(x, w1, s1, b1, wp, s2, b2, a1, a2, lib=lib),
+                              want):
+            return False
+    return True
+
+
 PINS = [pin_i8_hand, pin_i8_requant_near_ties, pin_i8_requant_closed_forms, pin_i8_dw_numpy,
-        pin_i8_pw_numpy, pin_i8_fused_numpy, pin_i8_fused_composition]
+        pin_i8_pw_numpy, pin_i8_fused_numpy, pin_i8_fused_composition, pin_i8_dense_numpy,
+        pin_i8_pwpw_composition]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -224,8 +288,15 @@ MUTANTS = {
         "t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *\n                                     (int64_t)wd[((size_t)c * k + j) * k + i];"),
     "pw_i8_weight_transposed": ("t += (int64_t)m[(size_t)q * Cm + c] * (int64_t)wp[(size_t)kk * Cm + c];",
                                 "t += (int64_t)m[(size_t)q * Cm + c] * (int64_t)wp[(size_t)c * K + kk];"),
-    "fused_i8_pw_bias_dropped": ("y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], b2[kk], act2);",
-                                 "y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], 0.0f, act2);"),
+    "fused_i8_pw_bias_dropped": (
+        "(int64_t)wp[(size_t)kk * C + c];\n                        y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], b2[kk], act2);",
+        "(int64_t)wp[(size_t)kk * C + c];\n                        y[IDX4(n, ho, wo, kk, Ho, Wo, K)] = requant_i8(t, s2[kk], 0.0f, act2);"),
+    "dense_i8_taps_swapped": (
+        "t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *\n                                     (int64_t)w1[IDX4(j, r, u, c, k, k, C)];",
+        "t += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *\n                                     (int64_t)w1[IDX4(j, u, r, c, k, k, C)];"),
+    "fused_dense_i8_pw_weight_transposed": (
+        "t += (int64_t)mid[j] * (int64_t)wp[(size_t)kk * Cm + j];",
+        "t += (int64_t)mid[j] * (int64_t)wp[(size_t)j * K + kk];"),
     "dw_i8_pad_sign": ("int hi = ho * s - p + i;\n                        if (hi < 0 || hi >= H) continue;\n                        for (int j = 0; j < k; j++) {\n                            int wi = wo * s - p + j;\n                            if (wi < 0 || wi >= W) continue;\n                            t += (int64_t)",
                        "int hi = ho * s + p + i;\n                        if (hi < 0 || hi >= H) continue;\n                        for (int j = 0; j < k; j++) {\n                            int wi = wo * s - p + j;\n                            if (wi < 0 || wi >= W) continue;\n                            t += (int64_t)"),
 }
