@@ -158,9 +158,9 @@ def oracle_step(oracle, wk, wl, case, nthreads: int):
     """One evaluation of the oracle's single-pass module on `case` (fp64, or the INT8 one) with
     `nthreads` OpenMP threads (the oracle's thread count is sticky, so every call sets it)."""
     if wl.dtype == "i8":
-        return lambda: oracle.fused_i8(case.x, case.w1, case.s1, case.b1, case.wp, case.s2,
-                                       case.b2, wl.act1, wl.act2, wl.stride, wl.pad,
-                                       nthreads=nthreads)
+        fn = oracle.fused_dense_i8 if wl.conv1 == "dense" else oracle.fused_i8
+        return lambda: fn(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2, wl.act1,
+                          wl.act2, wl.stride, wl.pad, nthreads=nthreads)
     f = case.f64()
     return lambda: oracle.fused(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
                                 wl.act1, wl.act2, wl.stride, wl.pad, conv1=wl.conv1,
@@ -291,7 +291,7 @@ def cpu_baseline(wk, wl, seconds: float) -> dict:
             "kind": "oracle", "images_per_s": round(ips, 4),
             "single_thread_images_per_s": round(1.0 / t_single, 4),
             "sample": f"{n_img} of {wl.n} images of {wl.name} x {reps} passes, "
-                      f"{'INT8 oracle_fused_i8' if wl.dtype == 'i8' else 'fp64 oracle_fused'}, "
+                      f"{'INT8 oracle' if wl.dtype == 'i8' else 'fp64 oracle_fused'}, "
                       f"{threads} OpenMP threads, {t:.2f} s"}
 
 

@@ -70,9 +70,11 @@ typedef enum fcm_status {
  * the intermediate are int8; scales and biases stay float32 and requantize each accumulator,
  *     q = clamp(rint(act(fmaf(s, (float)acc, b))), -128, 127)      (rint: ties to even),
  * the fma and the rounding in fp32 (|acc| < 2^24 for every supported shape, so acc converts
- * exactly).  INT8 runs only the depthwise module (FCM_CONV1_DEPTHWISE) on the tensor-core
- * kernels (C and K multiples of 16, K <= 256, ksize 1/3/5/7); other INT8 requests return
- * FCM_ERR_UNSUPPORTED.  The results are exact: the same integers on every run and in every
+ * exactly).  INT8 runs on the tensor-core kernels: the depthwise module (FCM_CONV1_DEPTHWISE;
+ * C <= 256 and K multiples of 16, K <= 256, ksize 1/3/5/7) and the PWPW module
+ * (FCM_CONV1_DENSE with ksize 1, pad 0: two 1x1 convolutions; C a multiple of 64, mid + k_out
+ * <= 256, and the tile's int8 and f16 input rings must fit in shared memory next to the
+ * weights, which holds up to C = 128); other INT8 requests return FCM_ERR_UNSUPPORTED.  The results are exact: the same integers on every run and in every
  * mode. */
 typedef enum fcm_dtype { FCM_F32 = 0, FCM_F16 = 1, FCM_BF16 = 2, FCM_I8 = 3 } fcm_dtype;
 typedef enum fcm_act { FCM_ACT_NONE = 0, FCM_ACT_RELU = 1, FCM_ACT_RELU6 = 2 } fcm_act;

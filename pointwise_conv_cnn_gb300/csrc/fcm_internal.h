@@ -90,6 +90,10 @@ fcm_status fcm_b2b_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, 
                         TcPlan *tc);
 fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_host);
 
+// tc_dwpw.cu: INT8 parts of a handle (stencil offsets of a depthwise w1_host, or none when
+// w1_host is NULL; the identity stencil and plan of the PW-only mode)
+fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host);
+
 // tc_pwdw.cu: 1x1 -> depthwise (PWDW) on tcgen05 + CUDA cores
 int fcm_pwdw_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);
 fcm_status fcm_pwdw_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,

@@ -22,6 +22,12 @@
 // warps 6-9 output epilogue.  Accumulators are double-buffered so conv1 of tile t overlaps
 // the epilogues of tile t-1.  In CONV1 mode (the layer-by-layer baseline) the mid warps store
 // the intermediate to HBM instead.  Every wait is bounded, as in the DW->PW kernels.
+//
+// INT8 (T = int8_t, k = 1: the PWPW module of section III-B's INT8 FCMs): the TMA loads the
+// int8 input tile into its own ring, warps 10-13 widen it exactly to the f16 A operand
+// (128-byte swizzled, as the TMA would have written it), and both GEMMs run as kind::f16 on
+// int8 values (exact: every partial sum stays below 2^22); the mid epilogue requantizes into the
+// f16 A2 operand, the output epilogue to int8 (64-byte rows, 64-byte swizzle).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <string.h>
@@ -42,6 +48,9 @@ constexpr int kMaxStages = 6;
 constexpr int kMidWarps = 4;
 constexpr int kOutWarps = 4;
 constexpr int kThreads = 32 * (2 + kMidWarps + kOutWarps);
+constexpr int kConvWarps = 4;                       // INT8: int8 -> f16 A operand
+constexpr int kFirstConvWarp = 2 + kMidWarps + kOutWarps;
+constexpr int kThreadsI8 = 32 * (kFirstConvWarp + kConvWarps);
 constexpr uint32_t kBlk = kTileM * 128;   // one 64-channel block of a 128-row operand
 
 enum Mode { FUSED = 0, CONV1 = 1 };
@@ -62,10 +71,15 @@ struct Args {
     uint32_t w1_bytes, w2_bytes, plane_bytes, in_stage_bytes, in_stage_stride;
     uint32_t off_w1, off_w2, off_a2, off_out, off_in, off_sb, off_bar;
     uint32_t out_bytes;     // one output staging tile (FUSED keeps two)
+    // INT8: the ring of int8 input tiles the TMA fills (planes of 64 channels x 64 bytes)
+    uint32_t off_in8, in8_stage_bytes, in8_stage_stride, plane8_bytes;
 };
 
 struct Bars {
-    uint32_t full, empty, acc1full, acc1empty, a2full, a2empty, acc2full, acc2empty, wbar, drain;
+    // full/empty: the input stage (INT8: full = int8 tile landed, empty = f16 A operand free);
+    // INT8 only: full1 = f16 A operand written, empty8 = int8 tile converted
+    uint32_t full, empty, acc1full, acc1empty, a2full, a2empty, acc2full, acc2empty, wbar, drain,
+        full1, empty8;
     __device__ Bars(uint32_t base) {
         full = base;
         empty = full + 8 * kMaxStages;
@@ -77,9 +91,11 @@ struct Bars {
         acc2empty = acc2full + 16;
         wbar = acc2empty + 16;
         drain = wbar + 8;
+        full1 = drain + 8;
+        empty8 = full1 + 8 * kMaxStages;
     }
 };
-constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 12 + 2) + 16;
+constexpr uint32_t kBarBytes = 8 * (4 * kMaxStages + 12 + 2) + 16;
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                        uint32_t d) {
@@ -117,48 +133,109 @@ __device__ __forceinline__ void emit16(const uint32_t (&rr)[16], int cc, const f
     sts128(base + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
 }
 
-// TMEM accumulator (128 lanes x ncols fp32, ncols a multiple of 16) -> scale/bias/act ->
-// 16-bit -> a 128-row, 128B-swizzled K-major image in shared memory (64-channel blocks of kBlk
-// bytes).  Two loads of 16 columns, then one wait.
-template <typename T, int ACT>
+// INT8, requantized to f16 (the A2 operand): the same 128-row, 128B-swizzled image.
+template <int ACT>
+__device__ __forceinline__ void emit16_i8_half(const uint32_t (&rr)[16], int cc, const float *sc_s,
+                                               const float *bi_s, uint32_t dst_s, int row) {
+    const uint32_t swz = (uint32_t)(row & 7);
+    uint32_t pk[8];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; i4++) {
+        const float4 s = *reinterpret_cast<const float4 *>(sc_s + cc + 4 * i4);
+        const float4 b = *reinterpret_cast<const float4 *>(bi_s + cc + 4 * i4);
+        pk[2 * i4] = I8::half2<ACT>(fmaf(s.x, __uint_as_float(rr[4 * i4]), b.x),
+                                    fmaf(s.y, __uint_as_float(rr[4 * i4 + 1]), b.y));
+        pk[2 * i4 + 1] = I8::half2<ACT>(fmaf(s.z, __uint_as_float(rr[4 * i4 + 2]), b.z),
+                                        fmaf(s.w, __uint_as_float(rr[4 * i4 + 3]), b.w));
+    }
+    const uint32_t base = dst_s + (uint32_t)(cc >> 6) * kBlk + (uint32_t)row * 128;
+    const uint32_t ch = (uint32_t)((cc & 63) >> 3);
+    sts128(base + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+    sts128(base + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
+}
+
+// INT8, requantized to int8 bytes: a 128-row image of 64-byte rows (64-channel blocks of
+// kTileM * 64 bytes), 64-byte swizzled (16-byte chunk c of row r at c ^ ((r >> 1) & 3)).
+template <int ACT>
+__device__ __forceinline__ void emit16_i8_bytes(const uint32_t (&rr)[16], int cc, const float *sc_s,
+                                                const float *bi_s, uint32_t dst_s, int row) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; i4++) {
+        const float4 s = *reinterpret_cast<const float4 *>(sc_s + cc + 4 * i4);
+        const float4 b = *reinterpret_cast<const float4 *>(bi_s + cc + 4 * i4);
+        pk[i4] = I8::bytes4<ACT>(fmaf(s.x, __uint_as_float(rr[4 * i4]), b.x),
+                                 fmaf(s.y, __uint_as_float(rr[4 * i4 + 1]), b.y),
+                                 fmaf(s.z, __uint_as_float(rr[4 * i4 + 2]), b.z),
+                                 fmaf(s.w, __uint_as_float(rr[4 * i4 + 3]), b.w));
+    }
+    const uint32_t base = dst_s + (uint32_t)(cc >> 6) * (kTileM * 64u) + (uint32_t)row * 64u;
+    const uint32_t ch = (uint32_t)((cc & 63) >> 4);
+    sts128(base + ((ch ^ (uint32_t)((row >> 1) & 3)) << 4), pk[0], pk[1], pk[2], pk[3]);
+}
+
+// What an accumulator becomes: the storage dtype (16-bit, 128B swizzle), or for INT8 the f16
+// A operand of the next GEMM or int8 bytes (64B swizzle).
+enum OutKind { OUT_STORAGE = 0, OUT_I8_HALF = 1, OUT_I8_BYTES = 2 };
+
+// TMEM accumulator (128 lanes x ncols fp32, ncols a multiple of 16) -> scale/bias/act -> the
+// image of OutKind in shared memory.  Two loads of 16 columns, then one wait.
+template <typename T, int KIND, int ACT>
 __device__ __forceinline__ void acc_to_smem_act(uint32_t taddr_row, int ncols, const float *sc_s,
                                                 const float *bi_s, uint32_t dst_s, int row) {
+    auto emit = [&](const uint32_t (&rr)[16], int cc) {
+        if constexpr (KIND == OUT_I8_HALF)
+            emit16_i8_half<ACT>(rr, cc, sc_s, bi_s, dst_s, row);
+        else if constexpr (KIND == OUT_I8_BYTES)
+            emit16_i8_bytes<ACT>(rr, cc, sc_s, bi_s, dst_s, row);
+        else
+            emit16<T, ACT>(rr, cc, sc_s, bi_s, dst_s, row);
+    };
     for (int c0 = 0; c0 < ncols; c0 += 32) {
         uint32_t ra[16], rb[16];
         const bool two = c0 + 16 < ncols;
         tmem_ld16(taddr_row + (uint32_t)c0, ra);
         if (two) tmem_ld16(taddr_row + (uint32_t)(c0 + 16), rb);
         tmem_ld_wait();
-        emit16<T, ACT>(ra, c0, sc_s, bi_s, dst_s, row);
-        if (two) emit16<T, ACT>(rb, c0 + 16, sc_s, bi_s, dst_s, row);
+        emit(ra, c0);
+        if (two) emit(rb, c0 + 16);
     }
 }
 
-template <typename T>
+template <typename T, int KIND>
 __device__ __forceinline__ void acc_to_smem(uint32_t taddr_row, int ncols, const float *sc_s,
                                             const float *bi_s, int act, uint32_t dst_s, int row) {
     with_act(act, [&](auto act_tag) {
-        acc_to_smem_act<T, decltype(act_tag)::value>(taddr_row, ncols, sc_s, bi_s, dst_s, row);
+        acc_to_smem_act<T, KIND, decltype(act_tag)::value>(taddr_row, ncols, sc_s, bi_s, dst_s,
+                                                            row);
     });
 }
 
 // Called by one thread after its warp group staged a tile: one TMA store per output row of
 // the tile and 64-channel block; rows past Ho are skipped, columns past Wo are clipped by the
 // tensor map.
+// (Staging rows of 64 channels: row_bytes 128 for 16-bit storage, 64 for int8.)
 __device__ __forceinline__ void store_tile(const Args &a, const CUtensorMap *map, uint32_t stage_s,
-                                           int nch, int n, int ho0) {
+                                           int nch, int n, int ho0, uint32_t row_bytes) {
     const int nkb = (nch + 63) / 64;
     for (int r = 0; r < a.TH; r++) {
         if (ho0 + r >= a.Ho) break;
         for (int kb = 0; kb < nkb; kb++)
-            tma_store_4d(map, stage_s + (uint32_t)kb * kBlk + (uint32_t)(r * a.P) * 128, kb * 64, 0,
-                         ho0 + r, n);
+            tma_store_4d(map, stage_s + (uint32_t)kb * kTileM * row_bytes + (uint32_t)(r * a.P) * row_bytes,
+                         kb * 64, 0, ho0 + r, n);
     }
     bulk_commit_group();
 }
 
 template <typename T, int KS, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(std::is_same<T, int8_t>::value ? kThreadsI8 : kThreads, 1)
+    b2b_kernel(const __grid_constant__ Args a) {
+    constexpr bool kI8 = std::is_same<T, int8_t>::value;
+    static_assert(!kI8 || KS == 1, "INT8 back-to-back runs k = 1 (two 1x1 convolutions)");
+    // what the epilogues write: the storage dtype, or for INT8 f16 A2 / int8 bytes
+    constexpr int kMidKind = !kI8 ? OUT_STORAGE : MODE == FUSED ? OUT_I8_HALF : OUT_I8_BYTES;
+    constexpr int kOutKind = kI8 ? OUT_I8_BYTES : OUT_STORAGE;
+    constexpr uint32_t kRowB = 64u * (uint32_t)sizeof(T);   // staging row bytes of stored data
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -185,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
         for (int s = 0; s < a.stages; s++) {
             mbar_init(bars.full + 8 * s, 1);
             mbar_init(bars.empty + 8 * s, 1);
+            if (kI8) {
+                mbar_init(bars.full1 + 8 * s, kConvWarps);
+                mbar_init(bars.empty8 + 8 * s, kConvWarps);
+            }
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(bars.acc1full + 8 * b, 1);
@@ -226,15 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
             const int t = (int)blockIdx.x + lt * (int)gridDim.x;
             const int n = t / a.tiles_per_img;
             const int ho0 = (t - n * a.tiles_per_img) * a.TH;
-            if (!mbar_wait(bars.empty + 8 * s, ph ^ 1u, abort_flag, a.err, lim)) {
+            // INT8: the int8 tile ring is free once the converters have read it
+            if (!mbar_wait((kI8 ? bars.empty8 : bars.empty) + 8 * s, ph ^ 1u, abort_flag, a.err, lim)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                const uint32_t dst = base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
-                mbar_arrive_expect_tx(bars.full + 8 * s, a.in_stage_bytes);
+                const uint32_t dst = kI8 ? base_s + a.off_in8 + (uint32_t)s * a.in8_stage_stride
+                                         : base_s + a.off_in + (uint32_t)s * a.in_stage_stride;
+                const uint32_t plane = kI8 ? a.plane8_bytes : a.plane_bytes;
+                mbar_arrive_expect_tx(bars.full + 8 * s, kI8 ? a.in8_stage_bytes : a.in_stage_bytes);
                 for (int kb = 0; kb < a.nkb_in; kb++)
-                    tma_load_4d(dst + (uint32_t)kb * a.plane_bytes, &a.tmap_in, bars.full + 8 * s,
+                    tma_load_4d(dst + (uint32_t)kb * plane, &a.tmap_in, bars.full + 8 * s,
                                 kb * 64, -a.pad, ho0 - a.pad, n);
             }
             issued++;
@@ -262,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
         for (int lt = 0; ok && lt <= last; lt++) {
             if (lt < my_tiles) {
                 const int b = lt & 1;
-                if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim) ||
+                if (!mbar_wait((kI8 ? bars.full1 : bars.full) + 8 * s, ph, abort_flag, a.err, lim) ||
                     !mbar_wait(bars.acc1empty + 8 * b, ((uint32_t)(lt >> 1) & 1u) ^ 1u, abort_flag,
                                a.err, lim)) {
                     ok = false;
@@ -355,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
             const uint32_t dst = MODE == FUSED
                                      ? base_s + a.off_a2 + (uint32_t)b * (uint32_t)a.nkb_mid * kBlk
                                      : base_s + a.off_out;
-            acc_to_smem<T>(taddr, a.Cm, s1_s, b1_s, a.act1, dst, row);
+            acc_to_smem<T, kMidKind>(taddr, a.Cm, s1_s, b1_s, a.act1, dst, row);
             tc_fence_before();
             fence_proxy_async_smem();
             __syncwarp();
@@ -367,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
                 if (issuer) {
                     const int t = (int)blockIdx.x + lt * (int)gridDim.x;
                     const int n = t / a.tiles_per_img;
-                    store_tile(a, &a.tmap_out, dst, a.Cm, n, (t - n * a.tiles_per_img) * a.TH);
+                    store_tile(a, &a.tmap_out, dst, a.Cm, n, (t - n * a.tiles_per_img) * a.TH, kRowB);
                 }
             }
         }
@@ -387,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc2_col + (uint32_t)b * (uint32_t)a.K;
             const uint32_t dst = base_s + a.off_out + (uint32_t)b * a.out_bytes;
-            acc_to_smem<T>(taddr, a.K, s2_s, b2_s, a.act2, dst, row);
+            acc_to_smem<T, kOutKind>(taddr, a.K, s2_s, b2_s, a.act2, dst, row);
             tc_fence_before();
             fence_proxy_async_smem();
             __syncwarp();
@@ -396,10 +480,59 @@ __global__ void __launch_bounds__(kThreads, 1) b2b_kernel(const __grid_constant_
             if (issuer) {
                 const int t = (int)blockIdx.x + lt * (int)gridDim.x;
                 const int n = t / a.tiles_per_img;
-                store_tile(a, &a.tmap_out, dst, a.K, n, (t - n * a.tiles_per_img) * a.TH);
+                store_tile(a, &a.tmap_out, dst, a.K, n, (t - n * a.tiles_per_img) * a.TH, kRowB);
             }
         }
         if (issuer) bulk_wait_group<0>();
+    } else if (kI8 && warp >= kFirstConvWarp && warp < kFirstConvWarp + kConvWarps) {
+        // ===================================================== INT8: int8 tile -> f16 A operand
+        // Thread p converts pixel row p of the tile (TH * P = 128 rows): per 64-channel plane,
+        // 64 int8 bytes -> 64 exact f16 values = one 128-byte row, 128B-swizzled as the tensor
+        // core reads it (16-byte chunk c at c ^ (p & 7)).
+        const int p = (warp - kFirstConvWarp) * 32 + lane;
+        const uint32_t swz = (uint32_t)(p & 7);
+        const __half2 bias2 = __float2half2_rn(I8::kBias);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int lt = 0; lt < my_tiles; lt++) {
+            // the int8 tile has landed, and the MMAs of this stage's previous tile are done
+            if (!mbar_wait(bars.full + 8 * s, ph, abort_flag, a.err, lim) ||
+                !mbar_wait(bars.empty + 8 * s, ph ^ 1u, abort_flag, a.err, lim))
+                break;
+            const uint8_t *src = base_g + a.off_in8 + (uint32_t)s * a.in8_stage_stride + (uint32_t)p * 64u;
+            const uint32_t dst = base_s + a.off_in + (uint32_t)s * a.in_stage_stride + (uint32_t)p * 128u;
+            for (int kb = 0; kb < a.nkb_in; kb++) {
+#pragma unroll
+                for (int h = 0; h < 4; h++) {   // 16 channels -> two 16-byte chunks of f16
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + (uint32_t)kb * a.plane8_bytes +
+                                                                     (uint32_t)h * 16u);
+                    uint32_t w[8];
+                    I8::widen4(v.x, w[0], w[1]);
+                    I8::widen4(v.y, w[2], w[3]);
+                    I8::widen4(v.z, w[4], w[5]);
+                    I8::widen4(v.w, w[6], w[7]);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {   // (1152 + x) - 1152 = x, exact in f16
+                        __half2 hv = *reinterpret_cast<__half2 *>(&w[i]);
+                        hv = __hsub2(hv, bias2);
+                        w[i] = *reinterpret_cast<uint32_t *>(&hv);
+                    }
+                    const uint32_t row_s = dst + (uint32_t)kb * a.plane_bytes;
+                    sts128(row_s + (((uint32_t)(2 * h) ^ swz) << 4), w[0], w[1], w[2], w[3]);
+                    sts128(row_s + (((uint32_t)(2 * h + 1) ^ swz) << 4), w[4], w[5], w[6], w[7]);
+                }
+            }
+            fence_proxy_async_smem();   // the f16 tile is read by the tensor core (async proxy)
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bars.full1 + 8 * s);
+                mbar_arrive(bars.empty8 + 8 * s);
+            }
+            if (++s == a.stages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
     }
 
     __syncwarp();
@@ -434,6 +567,7 @@ uint32_t align_up(uint32_t v, uint32_t al) { return (v + al - 1) / al * al; }
 struct Layout {
     uint32_t off_w1, off_w2, off_a2, off_out, off_in, off_sb, off_bar, out_bytes, plane_bytes,
         in_stage_bytes, in_stage_stride, w1_bytes, w2_bytes, total;
+    uint32_t off_in8, plane8_bytes, in8_stage_bytes, in8_stage_stride;   // INT8 input ring
     int stages;
 };
 
@@ -444,7 +578,9 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
     L.w1_bytes = (uint32_t)(ks * ks * nkb_in * cm) * 128u;
     L.w2_bytes = mode == FUSED ? (uint32_t)(nkb_mid * K) * 128u : 0u;
     const uint32_t a2 = mode == FUSED ? 2u * (uint32_t)nkb_mid * kBlk : 0u;
-    L.out_bytes = (uint32_t)(((mode == FUSED ? K : cm) + 63) / 64) * kBlk;
+    const bool i8 = d->dtype == FCM_I8;
+    // output staging: 64-channel blocks of kTileM rows of 128 (16-bit) or 64 (int8) bytes
+    L.out_bytes = (uint32_t)(((mode == FUSED ? K : cm) + 63) / 64) * (i8 ? kTileM * 64u : kBlk);
     const uint32_t out = (mode == FUSED ? 2u : 1u) * L.out_bytes;
     L.off_w1 = 0;
     L.off_w2 = align_up(L.w1_bytes, 1024);
@@ -454,13 +590,20 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
     L.plane_bytes = (uint32_t)(p.in_rows * p.tile_w) * 128u;
     L.in_stage_bytes = (uint32_t)nkb_in * L.plane_bytes;
     L.in_stage_stride = align_up(L.in_stage_bytes + 1024u, 1024);   // slack: taps read past the tile
+    if (i8) {
+        L.plane8_bytes = (uint32_t)(p.in_rows * p.tile_w) * 64u;
+        L.in8_stage_bytes = (uint32_t)nkb_in * L.plane8_bytes;
+        L.in8_stage_stride = align_up(L.in8_stage_bytes, 1024);
+    }
+    const uint32_t slot = L.in_stage_stride + L.in8_stage_stride;   // per stage: f16 (+ int8) tile
     const uint32_t sb = (uint32_t)(2 * cm + 2 * K) * 4;
     const uint32_t tail = align_up(sb, 16) + kBarBytes + 16 + 1024;
     int stages = kMaxStages;
     for (; stages >= 1; stages--)
-        if ((int)(L.off_in + (uint32_t)stages * L.in_stage_stride + tail) <= smem_cap) break;
+        if ((int)(L.off_in + (uint32_t)stages * slot + tail) <= smem_cap) break;
     L.stages = stages;
-    L.off_sb = L.off_in + (uint32_t)std::max(stages, 0) * L.in_stage_stride;
+    L.off_in8 = L.off_in + (uint32_t)std::max(stages, 0) * L.in_stage_stride;
+    L.off_sb = L.off_in + (uint32_t)std::max(stages, 0) * slot;
     L.off_bar = L.off_sb + align_up(sb, 16);
     L.total = L.off_bar + kBarBytes + 16 + 1024;
     return L;
@@ -485,6 +628,9 @@ int fcm_b2b_supported(const fcm_desc *d, int ho, int wo, int cm, const char **wh
     (void)ho;
     if (d->dtype == FCM_F32) return no("fp32 runs on CUDA cores");
     if (d->stride != 1) return no("dense conv1 on tensor cores needs stride 1");
+    // INT8: two 1x1 convolutions (PWPW); C, Cm <= 256 keep every partial sum below 2^22
+    if (d->dtype == FCM_I8 && (d->ksize != 1 || d->pad != 0))
+        return no("INT8 back-to-back takes k = 1 (the PWPW module)");
     if (d->ksize != 1 && d->ksize != 3 && d->ksize != 5) return no("dense conv1 ksize must be 1, 3 or 5");
     if (d->c % 64 != 0 || d->c > 256) return no("dense conv1 needs C a multiple of 64, at most 256");
     if (cm % 16 != 0 || d->k_out % 16 != 0) return no("mid and k_out must be multiples of 16");
@@ -514,6 +660,7 @@ fcm_status fcm_b2b_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, 
     t.threads = kThreads;
     t.ctas = (int)std::min<long long>(t.num_tiles, num_sms);
     t.tmem_cols = (int)pow2_cols(2 * (cm + d->k_out));
+    if (d->dtype == FCM_I8) t.threads = kThreadsI8;
     *p = t;
     return FCM_OK;
 }
@@ -522,24 +669,36 @@ fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_ho
     const fcm_desc &d = h->d;
     const int C = d.c, Cm = h->cm, K = d.k_out, ks = d.ksize;
     const int nkb_in = C / 64, nkb_mid = (Cm + 63) / 64;
+    const bool i8 = d.dtype == FCM_I8;
+    // 16-bit pattern of weight i: the storage value, or for INT8 the f16 of the int8 (exact)
+    auto w16 = [&](const void *base, size_t i) -> uint16_t {
+        if (i8) {
+            __half hv = __float2half_rn((float)static_cast<const signed char *>(base)[i]);
+            uint16_t b;
+            memcpy(&b, &hv, 2);
+            return b;
+        }
+        return static_cast<const uint16_t *>(base)[i];
+    };
     // conv1: for each tap, a B image with Cm rows (output channels) over the C input channels
-    std::vector<uint8_t> w1((size_t)ks * ks * nkb_in * Cm * 128, 0);
-    const uint16_t *src1 = static_cast<const uint16_t *>(w1_host);   // [Cm][ks][ks][C]
+    std::vector<uint8_t> w1((size_t)ks * ks * nkb_in * Cm * 128, 0);   // w1_host: [Cm][ks][ks][C]
     for (int j = 0; j < Cm; j++)
         for (int tap = 0; tap < ks * ks; tap++)
             for (int c = 0; c < C; c++) {
                 const int kb = c / 64;
                 const size_t blk = ((size_t)tap * nkb_in + kb) * Cm * 128;
                 const uint32_t off = fcm::tc::sw128_offset(j, c % 64, Cm, 2);
-                memcpy(&w1[blk + off], &src1[((size_t)j * ks * ks + tap) * C + c], 2);
+                const uint16_t v = w16(w1_host, ((size_t)j * ks * ks + tap) * C + c);
+                memcpy(&w1[blk + off], &v, 2);
             }
-    // conv2: K rows over Cm channels
+    // conv2: K rows over Cm channels (wp_host: [K][Cm])
     h->wp_img_bytes = (size_t)nkb_mid * K * 128;
     std::vector<uint8_t> w2(h->wp_img_bytes, 0);
-    const uint16_t *src2 = static_cast<const uint16_t *>(wp_host);   // [K][Cm]
     for (int n = 0; n < K; n++)
-        for (int c = 0; c < Cm; c++)
-            memcpy(&w2[fcm::tc::sw128_offset(n, c, K, 2)], &src2[(size_t)n * Cm + c], 2);
+        for (int c = 0; c < Cm; c++) {
+            const uint16_t v = w16(wp_host, (size_t)n * Cm + c);
+            memcpy(&w2[fcm::tc::sw128_offset(n, c, K, 2)], &v, 2);
+        }
     h->w1_img_bytes = w1.size();
     if (cudaMalloc(&h->w1_img, w1.size()) != cudaSuccess ||
         cudaMemcpy(h->w1_img, w1.data(), w1.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -547,6 +706,8 @@ fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_ho
         cudaMemcpy(h->wp_img, w2.data(), w2.size(), cudaMemcpyHostToDevice) != cudaSuccess)
         return fcm_fail(FCM_ERR_CUDA, "back-to-back weight images: %s",
                         cudaGetErrorString(cudaGetLastError()));
+    // INT8: the layer-by-layer second stage runs on the DW->PW kernel's identity stencil
+    if (i8) return fcm_i8_prepare(h, nullptr);
     return FCM_OK;
 }
 
@@ -557,7 +718,7 @@ cudaError_t launch_t(const Args &a, int ctas, uint32_t smem, cudaStream_t st) {
     auto k = b2b_kernel<T, KS, MODE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<ctas, kThreads, smem, st>>>(a);
+    k<<<ctas, std::is_same<T, int8_t>::value ? kThreadsI8 : kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -575,10 +736,12 @@ cudaError_t dispatch_ks(const Args &a, int ks, int mode, int ctas, uint32_t smem
     return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_dtype(const Args &a, bool f16, int ks, int mode, int ctas, uint32_t smem,
+cudaError_t dispatch_dtype(const Args &a, int dtype, int ks, int mode, int ctas, uint32_t smem,
                            cudaStream_t st) {
-    return f16 ? dispatch_ks<__half>(a, ks, mode, ctas, smem, st)
-               : dispatch_ks<__nv_bfloat16>(a, ks, mode, ctas, smem, st);
+    if (dtype == FCM_I8)
+        return ks == 1 ? dispatch_mode<int8_t, 1>(a, mode, ctas, smem, st) : cudaErrorInvalidValue;
+    return dtype == FCM_F16 ? dispatch_ks<__half>(a, ks, mode, ctas, smem, st)
+                            : dispatch_ks<__nv_bfloat16>(a, ks, mode, ctas, smem, st);
 }
 
 }  // namespace
@@ -594,29 +757,35 @@ cudaError_t launch_tc_b2b(const fcm_handle *h, int mode_in, const void *in, void
     if (L.stages < 2) return cudaErrorInvalidConfiguration;
     Args a;
     memset(&a, 0, sizeof(a));
-    const CUtensorMapDataType dt =
-        d.dtype == FCM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const bool i8 = d.dtype == FCM_I8;
+    const CUtensorMapDataType dt = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : d.dtype == FCM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t es = (cuuint64_t)fcm_dtype_bytes(d.dtype);
     {
+        // 16-bit: straight into the 128B-swizzled A operand; INT8: into the int8 ring (64-byte
+        // rows per 64-channel plane, unswizzled) that the converter warps read
         cuuint64_t gdim[4] = {(cuuint64_t)d.c, (cuuint64_t)d.w, (cuuint64_t)d.h, (cuuint64_t)d.n};
-        cuuint64_t gstride[3] = {(cuuint64_t)d.c * 2, (cuuint64_t)d.w * d.c * 2,
-                                 (cuuint64_t)d.h * d.w * d.c * 2};
+        cuuint64_t gstride[3] = {(cuuint64_t)d.c * es, (cuuint64_t)d.w * d.c * es,
+                                 (cuuint64_t)d.h * d.w * d.c * es};
         cuuint32_t box[4] = {64, (cuuint32_t)p.tile_w, (cuuint32_t)p.in_rows, 1};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         if (enc(&a.tmap_in, dt, 4, const_cast<void *>(in), gdim, gstride, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE,
+                i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
         const int ch = mode == FUSED ? d.k_out : h->cm;
         cuuint64_t gdim[4] = {(cuuint64_t)ch, (cuuint64_t)h->wo, (cuuint64_t)h->ho, (cuuint64_t)d.n};
-        cuuint64_t gstride[3] = {(cuuint64_t)ch * 2, (cuuint64_t)h->wo * ch * 2,
-                                 (cuuint64_t)h->ho * h->wo * ch * 2};
+        cuuint64_t gstride[3] = {(cuuint64_t)ch * es, (cuuint64_t)h->wo * ch * es,
+                                 (cuuint64_t)h->ho * h->wo * ch * es};
         cuuint32_t box[4] = {64, (cuuint32_t)p.tile_w, 1, 1};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         if (enc(&a.tmap_out, dt, 4, out, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                i8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     a.w1_img = static_cast<const uint8_t *>(h->w1_img);
@@ -645,7 +814,7 @@ cudaError_t launch_tc_b2b(const fcm_handle *h, int mode_in, const void *in, void
     a.act1 = d.act1;
     a.act2 = d.act2;
     a.tmem_cols = (uint32_t)p.tmem_cols;
-    a.idesc1 = idesc_f16(d.dtype == FCM_BF16, kTileM, h->cm);
+    a.idesc1 = idesc_f16(d.dtype == FCM_BF16, kTileM, h->cm);   // INT8: f16 operands
     a.idesc2 = idesc_f16(d.dtype == FCM_BF16, kTileM, d.k_out);
     a.w1_bytes = L.w1_bytes;
     a.w2_bytes = (uint32_t)h->wp_img_bytes;
@@ -660,6 +829,10 @@ cudaError_t launch_tc_b2b(const fcm_handle *h, int mode_in, const void *in, void
     a.off_in = L.off_in;
     a.off_sb = L.off_sb;
     a.off_bar = L.off_bar;
+    a.off_in8 = L.off_in8;
+    a.plane8_bytes = L.plane8_bytes;
+    a.in8_stage_bytes = L.in8_stage_bytes;
+    a.in8_stage_stride = L.in8_stage_stride;
     const int ctas = std::min(a.num_tiles, h->num_sms);
-    return dispatch_dtype(a, d.dtype == FCM_F16, d.ksize, mode, ctas, L.total, st);
+    return dispatch_dtype(a, d.dtype, d.ksize, mode, ctas, L.total, st);
 }

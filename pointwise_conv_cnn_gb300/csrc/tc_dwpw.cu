@@ -198,10 +198,11 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
 
 namespace {
 
-// INT8 handle parts: the per-channel stencil offsets 1152 * sum(taps), the identity stencil of
-// the PW-only mode and that mode's plan (the fused kernel with k = 1 over the intermediate).
+// The PW-only mode of an INT8 handle: the fused DW->PW kernel with an identity stencil over the
+// intermediate m [N, Ho, Wo, Cm].
 fcm_desc i8_pw_desc(const fcm_handle *h) {
     fcm_desc v = h->d;
+    v.conv1 = FCM_CONV1_DEPTHWISE;   // the identity stencil (also for the PWPW module's 2nd layer)
     v.h = h->ho;
     v.w = h->wo;
     v.c = h->cm;
@@ -215,14 +216,21 @@ fcm_desc i8_pw_desc(const fcm_handle *h) {
     return v;
 }
 
-fcm_status prepare_i8(fcm_handle *h, const void *w1_host) {
+}  // namespace
+
+// INT8 handle parts: the per-channel stencil offsets 1152 * sum(taps) (depthwise module only,
+// w1_host = its taps), the identity stencil of the PW-only mode and that mode's plan (the fused
+// DW->PW kernel with k = 1 over the intermediate).
+fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
     const int C = h->cm, KS = h->d.ksize;
-    const signed char *w8 = static_cast<const signed char *>(w1_host);
-    std::vector<float> q1(C), one(C, 1.0f), zero(C, 0.0f), idq(C, I8::kBias);
-    for (int c = 0; c < C; c++) {
-        int sum = 0;
-        for (int t = 0; t < KS * KS; t++) sum += w8[(size_t)c * KS * KS + t];
-        q1[c] = I8::kBias * (float)sum;   // |sum| <= 49 * 128: exact
+    std::vector<float> q1(C, 0.0f), one(C, 1.0f), zero(C, 0.0f), idq(C, I8::kBias);
+    if (w1_host) {
+        const signed char *w8 = static_cast<const signed char *>(w1_host);
+        for (int c = 0; c < C; c++) {
+            int sum = 0;
+            for (int t = 0; t < KS * KS; t++) sum += w8[(size_t)c * KS * KS + t];
+            q1[c] = I8::kBias * (float)sum;   // |sum| <= 49 * 128: exact
+        }
     }
     const __half h1 = __float2half_rn(1.0f);
     std::vector<__half> idtap(C, h1);
@@ -244,8 +252,6 @@ fcm_status prepare_i8(fcm_handle *h, const void *w1_host) {
         return fcm_fail(FCM_ERR_SMEM_BUDGET, "INT8 PW-only stage: no tile fits");
     return FCM_OK;
 }
-
-}  // namespace
 
 fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_host) {
     if (h->d.conv1 == FCM_CONV1_DENSE) return fcm_b2b_prepare(h, w1_host, wp_host);
@@ -279,7 +285,7 @@ fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_hos
     for (int c = 0; c < C; c++)
         for (int t = 0; t < KS * KS; t++) wdw[(size_t)t * C + c] = w16(w1_host, (size_t)c * KS * KS + t);
     if (i8) {
-        fcm_status st = prepare_i8(h, w1_host);
+        fcm_status st = fcm_i8_prepare(h, w1_host);
         if (st != FCM_OK) return st;
     }
     if (cudaMalloc(&h->wp_img, h->wp_img_bytes) != cudaSuccess ||

@@ -223,6 +223,9 @@ WORKLOADS = (
     # scales); ReLU after the depthwise layer, none after the pointwise one
     Workload("mobilenet_dwpw_i8", 64, 56, 56, 128, 128, "dw", 3, 1, 1, "relu", "none", "i8",
              "int8"),
+    # the PWPW pair in INT8: 1x1 64 -> 128 (ReLU), 1x1 128 -> 64 (none)
+    Workload("pwpw_i8", 64, 56, 56, 64, 64, "dense", 1, 1, 0, "relu", "none", "i8", "int8",
+             mid=128),
 )
 BY_NAME = {w.name: w for w in WORKLOADS}
 

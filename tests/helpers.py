@@ -73,9 +73,9 @@ def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
 def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.ndarray:
     wl = case.wl
     if wl.dtype == "i8":   # int8 results, as float64 for the shared comparisons
-        return oracle.fused_i8(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2,
-                               wl.act1, wl.act2, wl.stride, wl.pad,
-                               nthreads=nthreads).astype(np.float64)
+        fn = oracle.fused_dense_i8 if wl.conv1 == "dense" else oracle.fused_i8
+        return fn(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2, wl.act1, wl.act2,
+                  wl.stride, wl.pad, nthreads=nthreads).astype(np.float64)
     f = case.f64()
     if wl.conv1 == "pwdw":
         return oracle.pwdw(f["x"], f["w1"], f["s1"], f["b1"], f["wp"], f["s2"], f["b2"],
@@ -87,8 +87,8 @@ def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.nda
 def oracle_conv1(case: wk.Case) -> np.ndarray:
     wl = case.wl
     if wl.dtype == "i8":
-        return oracle.dw_i8(case.x, case.w1, case.s1, case.b1, wl.act1, wl.stride,
-                            wl.pad).astype(np.float64)
+        fn = oracle.dense_i8 if wl.conv1 == "dense" else oracle.dw_i8
+        return fn(case.x, case.w1, case.s1, case.b1, wl.act1, wl.stride, wl.pad).astype(np.float64)
     f = case.f64()
     if wl.conv1 == "pwdw":   # the 1x1 layer, over the input's extent
         return oracle.pw(f["x"], f["w1"], f["s1"], f["b1"], wl.act1)

@@ -226,7 +226,8 @@ def test_int8_edge_shapes(cuda, shape):
 
 def test_int8_shapes_refused(cuda):
     """INT8 requests outside the tensor-core kernels fail with FCM_ERR_UNSUPPORTED."""
-    for kw in ({"conv1": "dense", "mid": 32}, {"c": 512, "k_out": 64}):
+    for kw in ({"conv1": "dense", "mid": 32}, {"c": 512, "k_out": 64},
+               {"conv1": "pwdw", "mid": 32}):
         wl = wk.Workload("i8_no", 1, 8, 8, kw.get("c", 32), kw.get("k_out", 32),
                          kw.get("conv1", "dw"), 3, 1, 1, "relu", "none", "i8", "int8",
                          mid=kw.get("mid", 0))
@@ -329,3 +330,37 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda):
     case = wk.make_case(wl)
     got, _ = run_case(case, "fused")
     assert_bitexact(got, oracle_fused(case), "i8")
+
+
+I8_PWPW_EDGE = [  # (N, H, W, C, Cm, K, act1, act2): the INT8 PWPW module (two 1x1 convolutions)
+    (2, 9, 13, 64, 64, 64, "relu", "none"),
+    (1, 11, 60, 128, 64, 128, "none", "relu6"),
+    (3, 7, 100, 64, 32, 48, "relu6", "relu"),
+    (1, 5, 21, 128, 64, 128, "relu", "none"),
+    (2, 1, 1, 64, 16, 16, "none", "none"),
+]
+
+
+@pytest.mark.parametrize("shape", I8_PWPW_EDGE, ids=lambda s: "x".join(map(str, s[:6])))
+def test_int8_pwpw_edge_shapes(cuda, shape):
+    """INT8 1x1 -> 1x1 on the back-to-back kernel (int8 tiles widened to f16 by converter
+    warps): bit-exact with the oracle fused, layer by layer, first layer alone, and the second
+    layer on the oracle's intermediate; pitches of 64 and 128 columns, C up to 128 (the int8
+    and the f16 input rings of wider layers do not fit next to the weights)."""
+    import torch
+    N, H, W, C, Cm, K, a1, a2 = shape
+    wl = wk.Workload("i8_pwpw", N, H, W, C, K, "dense", 1, 1, 0, a1, a2, "i8", "int8", mid=Cm)
+    case = wk.make_case(wl, seed=93)
+    mod = make_module(case, "tc")
+    ref = oracle_fused(case)
+    for mode in ("fused", "unfused"):
+        got, _ = run_case(case, mode, module=mod)
+        assert_bitexact(got, ref, "i8")
+    m_ref = oracle_conv1(case)
+    m_gpu, _ = run_case(case, "conv1", module=mod)
+    assert_bitexact(m_gpu, m_ref, "i8")
+    y = empty(wl.shapes()["y"], "i8", fill=float("nan"))
+    mod.run(to_device(m_ref.astype(np.int8), "i8"), y, "pw")
+    torch.cuda.synchronize()
+    mod.check()
+    assert_bitexact(to_host(y, "i8"), oracle_pw(case, m_ref), "i8")
