@@ -139,3 +139,17 @@ def test_int8_plans_and_refusals():
     with pytest.raises(fcm.FcmError) as e:
         fcm.fcm_plan_desc(fcm.desc_from_workload(i8, kernel="simt"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_plans_fit_the_gb300_limits(wl):
+    """Every workload's plan (planned on the host for 152 SMs and 227 KB of shared memory a
+    block) fits the limits the kernels are launched under: dynamic shared memory, whole warps,
+    at most 1024 threads, a persistent grid of at most one CTA per SM, at least two stages."""
+    info = fcm.fcm_plan_desc(fcm.desc_from_workload(wl), 152, 232448)
+    assert info["smem_bytes"] <= 232448
+    assert info["threads"] % 32 == 0 and 0 < info["threads"] <= 1024
+    assert 0 < info["ctas"] <= 152 * (8 if info["kernel"] == 1 else 1)
+    if info["kernel"] == 2:
+        assert info["stages"] >= 2
+        assert info["tile_h"] * info["tile_w"] <= 128 or wl.conv1 == "pwdw"
