@@ -40,3 +40,15 @@ def test_reference_arm_line(workload, dtype):
 
 def test_reference_arm_other_ranks_are_silent():
     assert run_reference("tiny_dwpw_f32", {"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_gpu_arm_fails_loudly_without_a_gpu():
+    """No CPU fallback: without a GPU the measured arm exits non-zero and prints no result."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", "--warmup",
+                        "1", "--no-cpu-baseline"], capture_output=True, text=True, cwd=ROOT,
+                       timeout=600)
+    assert r.returncode != 0
+    assert not any(l.startswith("{") for l in r.stdout.splitlines())
