@@ -132,3 +132,33 @@ def test_int8_bit_width_changes_the_fusion_decision():
         assert plans[0]["fuse_with_next"] == fused == ref[0]["fuse_with_next"], elem_bytes
         assert total == ref_total
     assert fcm.fcm_fuse_plan(layers, 1, 1, l1, 1)[1] == 17408
+
+
+def inverted_residual_chain(blocks=4):
+    """A MobileNetV2-style stack written here (not a model's table): per block a 1x1 expansion
+    (x6), a 3x3 depthwise layer (stride 2 or 1) and a 1x1 projection, from 112x112x16."""
+    layers, H, c = [], 112, 16
+    for cout, s in ((24, 2), (24, 1), (32, 2), (32, 1))[:blocks]:
+        e = 6 * c
+        layers.append(dict(kind="pw", h=H, w=H, c=c, k_out=e))
+        layers.append(dict(kind="dw", h=H, w=H, c=e, ksize=3, stride=s, pad=1))
+        H = (H + 2 - 3) // s + 1
+        layers.append(dict(kind="pw", h=H, w=H, c=e, k_out=cout))
+        c = cout
+    return layers
+
+
+def test_int8_chain_fuses_more_kinds_of_pairs():
+    """Section V-B on a chain: with 64 KiB of L1 and 152 SMs, FP32 fuses only the four
+    expansion -> depthwise pairs (PWDW), while INT8's smaller elements also admit a PWPW and a
+    DWPW fusion; the literal model makes the same decisions."""
+    layers = inverted_residual_chain()
+    kinds = {}
+    for e in (4, 1):
+        plans, total = fcm.fcm_fuse_plan(layers, 1, 152, 64 * 1024, e)
+        ref, ref_total = pm.plan_chain(layers, 1, 152, 64 * 1024 // e)
+        assert total == ref_total
+        assert [p["fuse_with_next"] for p in plans] == [r["fuse_with_next"] for r in ref]
+        kinds[e] = sorted(p["fcm_module"] for p in plans if p["fuse_with_next"])
+    assert kinds[4] == ["pwdw"] * 4
+    assert kinds[1] == sorted(["pwdw"] * 3 + ["pwpw", "dwpw"])
