@@ -153,3 +153,17 @@ def test_plans_fit_the_gb300_limits(wl):
     if info["kernel"] == 2:
         assert info["stages"] >= 2
         assert info["tile_h"] * info["tile_w"] <= 128 or wl.conv1 == "pwdw"
+
+
+@pytest.mark.parametrize("n,ok", [(1 << 18, True), (1 << 24, False)])
+def test_huge_batches_plan_or_refuse_cleanly(n, ok):
+    """A batch of 2^18 MobileNet images plans (7.3 M tiles, 32-bit tile indices); 2^24 images
+    (6.7e12 input elements, above the 2^40 guard) is refused with FCM_ERR_UNSUPPORTED."""
+    wl = wk.BY_NAME["mobilenet_dwpw_f16"].with_(n=n)
+    if ok:
+        info = fcm.fcm_plan_desc(fcm.desc_from_workload(wl), 152, 232448)
+        assert info["num_tiles"] == n * 28 and info["ctas"] == 152
+    else:
+        with pytest.raises(fcm.FcmError) as e:
+            fcm.fcm_plan_desc(fcm.desc_from_workload(wl), 152, 232448)
+        assert e.value.status == 2
