@@ -213,7 +213,9 @@ FCM_API void fcm_destroy(fcm_handle *h);
 FCM_API const char *fcm_last_error(void);
 
 /* ---- FusePlanner cost models, section IV (element counts per image; exported for tests). */
-/* Eq. 1: halo elements per channel re-read across tiles. */
+/* Eq. 1: halo elements per channel re-read across tiles.  A filter narrower than the stride
+ * (windows that do not overlap) counts 0 halo columns/rows, not a negative number.  Returns -1
+ * for a tile extent <= 0. */
 FCM_API long long fcm_model_overlap(long long channel_w, long long channel_h, long long tile_w,
                             long long tile_h, long long filter_w, long long filter_h,
                             long long strides);

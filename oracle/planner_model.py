@@ -28,9 +28,12 @@ def ceil_div(a: int, b: int) -> int:
 
 def overlap(channel_w: int, channel_h: int, tile_w: int, tile_h: int,
             filter_w: int, filter_h: int, strides: int) -> int:
-    """Equation 1: halo elements (per channel) re-read across neighbouring tiles."""
-    return ((ceil_div(channel_w, tile_w) - 1) * (filter_w - strides) * channel_h
-            + (ceil_div(channel_h, tile_h) - 1) * (filter_h - strides) * channel_w)
+    """Equation 1: halo elements (per channel) re-read across neighbouring tiles.  The
+    equation is stated for overlapping windows (filter at least as wide as the stride); a
+    narrower filter leaves gaps and re-reads nothing, so FilterW - Strides is taken as 0 there
+    instead of a negative count."""
+    return ((ceil_div(channel_w, tile_w) - 1) * max(filter_w - strides, 0) * channel_h
+            + (ceil_div(channel_h, tile_h) - 1) * max(filter_h - strides, 0) * channel_w)
 
 
 def pw_gma(weights_sz: int, weights_tile_sz: int, ifms_sz: int, ofms_sz: int,

@@ -20,8 +20,12 @@ long long fcm_model_overlap(long long channel_w, long long channel_h, long long 
                             long long tile_h, long long filter_w, long long filter_h,
                             long long strides) {
     if (tile_w <= 0 || tile_h <= 0) return -1;
-    return (ceil_div_ll(channel_w, tile_w) - 1) * (filter_w - strides) * channel_h +
-           (ceil_div_ll(channel_h, tile_h) - 1) * (filter_h - strides) * channel_w;
+    // a filter narrower than the stride leaves gaps between neighbouring windows: no element
+    // is read twice, so the halo width is clamped at zero rather than going negative
+    long long halo_w = filter_w > strides ? filter_w - strides : 0;
+    long long halo_h = filter_h > strides ? filter_h - strides : 0;
+    return (ceil_div_ll(channel_w, tile_w) - 1) * halo_w * channel_h +
+           (ceil_div_ll(channel_h, tile_h) - 1) * halo_h * channel_w;
 }
 
 long long fcm_model_pw_gma(long long weights_sz, long long weights_tile_sz, long long ifms_sz,

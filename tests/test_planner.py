@@ -20,6 +20,11 @@ def test_eq1_overlap_by_hand():
     assert fcm.fcm_model_overlap(56, 56, 28, 14, 3, 3, 1) == 448
     # one tile: no overlap
     assert fcm.fcm_model_overlap(56, 56, 56, 56, 3, 3, 1) == 0
+    # filter no wider than the stride: windows of neighbouring tiles share nothing
+    for f in (pm.overlap, fcm.fcm_model_overlap):
+        assert f(9, 9, 2, 2, 1, 1, 2) == 0 and f(8, 8, 4, 4, 2, 2, 2) == 0
+        # 3 wide at stride 2: one shared column per tile boundary, (ceil(9/4)-1)*1*9 = 18 per axis
+        assert f(9, 9, 4, 4, 3, 3, 2) == 36
 
 
 def test_eq2_eq3_dwpw_by_hand():
