@@ -29,6 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfcm.so")
 
 FCM_OK = 0
+FCM_ERR_INVALID_ARG = 1
 STATUS_NAMES = {0: "FCM_OK", 1: "FCM_ERR_INVALID_ARG", 2: "FCM_ERR_UNSUPPORTED",
                 3: "FCM_ERR_ALIGNMENT", 4: "FCM_ERR_SMEM_BUDGET", 5: "FCM_ERR_CUDA",
                 6: "FCM_ERR_TIMEOUT", 7: "FCM_ERR_DEVICE_FAULT", 8: "FCM_ERR_NO_DEVICE"}
@@ -266,6 +267,33 @@ def fcm_fuse_plan(layers, batch: int = 1, num_sms: int = 152, l1_bytes: int = 23
     return [o.as_dict() for o in out], total.value
 
 
+def mode_bytes(desc: FcmDesc) -> dict[int, tuple[int, int]]:
+    """Bytes each fcm_run mode reads and writes: {mode: (input bytes, output bytes)}."""
+    x, m, y = fcm_tensor_bytes(desc)
+    return {MODES["fused"]: (x, y), MODES["conv1"]: (x, m), MODES["pw"]: (m, y),
+            MODES["unfused"]: (x, y)}
+
+
+def check_run_buffers(need: dict, mode: int, inp, out, on_device: bool) -> None:
+    """Refuse tensors the library would read or write past: the C ABI takes bare pointers, so
+    the binding checks what only it can see -- device, contiguity and size."""
+    sizes = need.get(mode)
+    if sizes is None:
+        raise FcmError(FCM_ERR_INVALID_ARG, f"mode {mode}")
+    if (inp.is_cuda == on_device and out.is_cuda == on_device and inp.is_contiguous()
+            and out.is_contiguous() and inp.nbytes >= sizes[0] and out.nbytes >= sizes[1]):
+        return
+    where = "a CUDA" if on_device else "a host"
+    for t, nbytes, what in ((inp, sizes[0], "input"), (out, sizes[1], "output")):
+        if bool(t.is_cuda) != on_device:
+            raise FcmError(FCM_ERR_INVALID_ARG, f"{what} must be {where} tensor")
+        if not t.is_contiguous():
+            raise FcmError(FCM_ERR_INVALID_ARG, f"{what} must be contiguous (NHWC)")
+        if t.nbytes < nbytes:
+            raise FcmError(FCM_ERR_INVALID_ARG,
+                           f"{what} holds {t.nbytes} bytes; the mode needs {nbytes}")
+
+
 class FusedConvModule:
     """Owns one FCM handle.  Weights are torch tensors or numpy arrays in the storage dtype
     (bf16 may be given as uint16 bit patterns, INT8 as int8); scales/biases float32."""
@@ -287,11 +315,14 @@ class FusedConvModule:
         self.handle = fcm_create(desc, addr(w1), addr(wp), addr(s1), addr(b1), addr(s2),
                                  addr(b2))
         self.plan = fcm_plan(self.handle)
+        self.mode_bytes = mode_bytes(desc)
 
     def run(self, inp, out, mode: str | int = "fused", stream=None) -> None:
-        """Enqueue on `stream` (torch.cuda.Stream, raw handle int, or None = current stream)."""
+        """Enqueue on `stream` (torch.cuda.Stream, raw handle int, or None = current stream).
+        `inp`/`out` are contiguous CUDA tensors holding at least the mode's bytes."""
         import torch
         m = MODES[mode] if isinstance(mode, str) else mode
+        check_run_buffers(self.mode_bytes, m, inp, out, on_device=True)
         if stream is None:
             s = torch.cuda.current_stream().cuda_stream
         elif hasattr(stream, "cuda_stream"):
@@ -301,8 +332,10 @@ class FusedConvModule:
         fcm_run(self.handle, m, inp.data_ptr(), out.data_ptr(), s)
 
     def run_host(self, host_in, host_out, mode: str | int = "fused", stream=None) -> None:
+        """`host_in`/`host_out`: contiguous host tensors (pinned for overlapped copies)."""
         import torch
         m = MODES[mode] if isinstance(mode, str) else mode
+        check_run_buffers(self.mode_bytes, m, host_in, host_out, on_device=False)
         s = (torch.cuda.current_stream().cuda_stream if stream is None
              else getattr(stream, "cuda_stream", stream))
         fcm_run_host(self.handle, m, host_in.data_ptr(), host_out.data_ptr(), s)
