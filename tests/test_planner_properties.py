@@ -141,6 +141,9 @@ def check_plan(kw, info):
         assert info["stages"] >= 2
         assert 0 < info["ctas"] <= min(info["num_tiles"], NUM_SMS)
         assert info["num_tiles"] == N * -(-ho // th) * -(-wo // tw)   # covers every pixel
+        # TMA boxes start at channel offsets that are multiples of the chunk: the innermost
+        # coordinate times the element size must be a multiple of 16 bytes
+        assert info["chunk_c"] > 0 and (info["chunk_c"] * ESIZE[kw["dtype"]]) % 16 == 0
         if kw["conv1"] == "dw":
             assert th * tw <= 128 and cm % info["chunk_c"] == 0
     else:
