@@ -8,8 +8,9 @@ from it.
 The arithmetic lives in ``fcm_oracle.c`` (plain loops, fp64).  This module only builds that
 file with gcc, loads it with ctypes and marshals numpy arrays.  Inputs of any float dtype are
 upcast to float64 exactly before the call; outputs are float64.  The INT8 functions
-(``dw_i8``, ``pw_i8``, ``fused_i8``, ``dense_i8``, ``fused_dense_i8``) take int8 activations and weights and fp32 scales and
-biases, and return int8 (section III-B's INT8 FCMs).
+(``dw_i8``, ``pw_i8``, ``fused_i8``, ``dense_i8``, ``fused_dense_i8``, ``pwdw_i8``) take int8
+activations and weights and fp32 scales and biases, and return int8 (section III-B's INT8
+FCMs).
 
 Definitions followed (see the C file for the full list): "Fusing Depthwise and Pointwise
 Convolutions for Efficient Inference on GPUs", section II-B (DW and PW convolutions),
@@ -70,9 +71,11 @@ def bind(path: str):
     lib.oracle_requant_i8.argtypes = [ctypes.c_longlong, ctypes.c_float, ctypes.c_float, i]
     lib.oracle_dense_i8.argtypes = [i] * 8 + [bp, bp, fp, fp, i, bp, i]
     lib.oracle_fused_dense_i8.argtypes = [i] * 9 + [bp, bp, fp, fp, i, bp, fp, fp, i, bp, i]
+    lib.oracle_pwdw_i8.argtypes = [i] * 8 + [bp, bp, fp, fp, i, bp, fp, fp, i, bp, i]
     for f in (lib.oracle_dw, lib.oracle_pw, lib.oracle_dense, lib.oracle_fused, lib.oracle_pwdw,
               lib.oracle_max_threads, lib.oracle_dw_i8, lib.oracle_pw_i8, lib.oracle_fused_i8,
-              lib.oracle_requant_i8, lib.oracle_dense_i8, lib.oracle_fused_dense_i8):
+              lib.oracle_requant_i8, lib.oracle_dense_i8, lib.oracle_fused_dense_i8,
+              lib.oracle_pwdw_i8):
         f.restype = ctypes.c_int
     return lib
 
@@ -306,6 +309,26 @@ def fused_dense_i8(x, w1, s1, b1, wp, s2, b2, act1="none", act2="none", stride=1
                                           _p32(b2), ACT[act2], _p8(y), nthreads)
     if rc != 0:
         raise ValueError("oracle_fused_dense_i8: invalid shape")
+    return y
+
+
+def pwdw_i8(x, wq, s1, b1, wd2, s2, b2, act1="none", act2="none", stride=1, pad=0,
+            nthreads=0, lib=None) -> np.ndarray:
+    """INT8 PWDW module in one pass (int8 intermediate, recomputed under each depthwise tap):
+    x [N,H,W,C], wq [Cm,C], wd2 [Cm,k,k] int8; s1/b1, s2/b2 [Cm] fp32 -> y [N,Ho,Wo,Cm] int8."""
+    x, wq, wd2 = _i8(x), _i8(wq), _i8(wd2)
+    s1, b1, s2, b2 = map(_f32, (s1, b1, s2, b2))
+    N, H, W, C = x.shape
+    Cm, k = wd2.shape[0], wd2.shape[1]
+    assert wq.shape == (Cm, C) and wd2.shape == (Cm, k, k)
+    assert all(v.shape == (Cm,) for v in (s1, b1, s2, b2))
+    Ho, Wo = out_extent(H, k, stride, pad), out_extent(W, k, stride, pad)
+    y = np.empty((N, Ho, Wo, Cm), np.int8)
+    rc = _load(lib).oracle_pwdw_i8(N, H, W, C, Cm, k, stride, pad, _p8(x), _p8(wq), _p32(s1),
+                                   _p32(b1), ACT[act1], _p8(wd2), _p32(s2), _p32(b2), ACT[act2],
+                                   _p8(y), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_pwdw_i8: invalid shape")
     return y
 
 

@@ -502,3 +502,41 @@ int oracle_fused_dense_i8(int N, int H, int W, int C, int Cm, int K, int k, int 
     }
     return failed ? -1 : 0;
 }
+
+/* The INT8 PWDW module as its own single pass (section II-D's PWDW with section III-B's INT8
+ * buffers): for every output pixel and channel j, the int8 intermediate under each depthwise
+ * tap is the 1x1 convolution of the input pixel there, requantized on the spot; taps that
+ * fall in the padding read int8 zero, because the padding belongs to the depthwise layer's
+ * input.  It does not call oracle_pw_i8/oracle_dw_i8.
+ * x [N][H][W][C], wq [Cm][C], wd2 [Cm][k][k] int8; s1/b1, s2/b2 [Cm] -> y [N][Ho][Wo][Cm]. */
+int oracle_pwdw_i8(int N, int H, int W, int C, int Cm, int k, int s, int p,
+                   const int8_t *x, const int8_t *wq, const float *s1, const float *b1, int act1,
+                   const int8_t *wd2, const float *s2, const float *b2, int act2,
+                   int8_t *y, int nthreads) {
+    int Ho = out_extent(H, k, s, p), Wo = out_extent(W, k, s, p);
+    if (N < 0 || C < 1 || Cm < 1 || Ho < 1 || Wo < 1) return -1;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int n = 0; n < N; n++)
+        for (int ho = 0; ho < Ho; ho++)
+            for (int wo = 0; wo < Wo; wo++)
+                for (int j = 0; j < Cm; j++) {
+                    int64_t t = 0;
+                    for (int i = 0; i < k; i++) {
+                        int hi = ho * s - p + i;
+                        if (hi < 0 || hi >= H) continue;
+                        for (int u = 0; u < k; u++) {
+                            int wi = wo * s - p + u;
+                            if (wi < 0 || wi >= W) continue;
+                            int64_t q = 0;
+                            for (int c = 0; c < C; c++)
+                                q += (int64_t)x[IDX4(n, hi, wi, c, H, W, C)] *
+                                     (int64_t)wq[(size_t)j * C + c];
+                            int8_t mval = requant_i8(q, s1[j], b1[j], act1);
+                            t += (int64_t)mval * (int64_t)wd2[((size_t)j * k + i) * k + u];
+                        }
+                    }
+                    y[IDX4(n, ho, wo, j, Ho, Wo, Cm)] = requant_i8(t, s2[j], b2[j], act2);
+                }
+    return 0;
+}

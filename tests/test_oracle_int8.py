@@ -9,7 +9,8 @@
 * the convolutions against a direct numpy formulation in int64 (sliding windows of the
   zero-padded input, an integer matrix product for the 1x1);
 * fused == pointwise(depthwise(x)) exactly (the single-pass function against the two layer
-  functions);
+  functions), and the PWDW module == depthwise(pointwise(x)) likewise, with a hand case that
+  separates padding the intermediate from padding the input;
 * planted mistakes in a copy of the oracle source must fail at least one pin.
 """
 import numpy as np
@@ -243,9 +244,66 @@ def pin_i8_pwpw_composition(lib=None):
     return True
 
 
+PWDW_CASES = [  # (N, H, W, C, Cm, k, stride, pad, act1, act2): 1x1 C -> Cm, then depthwise
+    (1, 5, 6, 3, 4, 3, 1, 1, "relu6", "relu"),
+    (2, 6, 5, 4, 3, 3, 2, 1, "none", "relu6"),
+    (1, 7, 6, 2, 5, 5, 1, 2, "relu", "none"),
+    (1, 4, 4, 3, 2, 1, 1, 0, "none", "none"),
+]
+
+
+def draw_pwdw(r, N, H, W, C, Cm, k):
+    x = r.integers(-128, 128, (N, H, W, C)).astype(np.int8)
+    wq = r.integers(-128, 128, (Cm, C)).astype(np.int8)
+    wd2 = r.integers(-128, 128, (Cm, k, k)).astype(np.int8)
+    s1 = (r.uniform(0.5, 1.5, Cm) * 32 / (74 * 74 * np.sqrt(C))).astype(np.float32)
+    b1 = r.uniform(-4, 4, Cm).astype(np.float32)
+    s2 = (r.uniform(0.5, 1.5, Cm) * 32 / (74 * 23 * k)).astype(np.float32)
+    b2 = r.uniform(-4, 4, Cm).astype(np.float32)
+    return x, wq, s1, b1, wd2, s2, b2
+
+
+def pin_i8_pwdw_numpy(lib=None):
+    """The INT8 PWDW module against int64 numpy: the 1x1 over the input's extent, requantized,
+    then the depthwise layer over that int8 intermediate zero-padded."""
+    r = rng(31)
+    for (N, H, W, C, Cm, k, st, p, a1, a2) in PWDW_CASES:
+        x, wq, s1, b1, wd2, s2, b2 = draw_pwdw(r, N, H, W, C, Cm, k)
+        want = dw_np(pw_np(x, wq, s1, b1, a1), wd2, s2, b2, a2, st, p)
+        got = oracle.pwdw_i8(x, wq, s1, b1, wd2, s2, b2, a1, a2, st, p, lib=lib)
+        if not np.array_equal(got, want):
+            return False
+    return True
+
+
+def pin_i8_pwdw_composition(lib=None):
+    """pwdw_i8 == dw_i8(pw_i8(x)) (the oracle's own two layer functions)."""
+    r = rng(37)
+    for (N, H, W, C, Cm, k, st, p, a1, a2) in PWDW_CASES:
+        x, wq, s1, b1, wd2, s2, b2 = draw_pwdw(r, N, H, W, C, Cm, k)
+        m = oracle.pw_i8(x, wq, s1, b1, a1, lib=lib)
+        want = oracle.dw_i8(m, wd2, s2, b2, a2, st, p, lib=lib)
+        if not np.array_equal(oracle.pwdw_i8(x, wq, s1, b1, wd2, s2, b2, a1, a2, st, p, lib=lib),
+                              want):
+            return False
+    return True
+
+
+def pin_i8_pwdw_padding_by_hand(lib=None):
+    """One pixel x = 2, 1x1 weight 3, bias 4: the intermediate is 3*2 + 4 = 10.  A 3x3
+    all-ones depthwise filter with pad 1 sees only that pixel, so y = 10.  Padding the input
+    instead (the 1x1 of a zero pixel is the bias, 4, at each of the eight border taps) would
+    give 10 + 8*4 = 42."""
+    y = oracle.pwdw_i8(np.full((1, 1, 1, 1), 2, np.int8), np.full((1, 1), 3, np.int8), [1.0],
+                       [4.0], np.ones((1, 3, 3), np.int8), [1.0], [0.0], "none", "none", 1, 1,
+                       lib=lib)
+    return y.shape == (1, 1, 1, 1) and int(y[0, 0, 0, 0]) == 10
+
+
 PINS = [pin_i8_hand, pin_i8_requant_near_ties, pin_i8_requant_closed_forms, pin_i8_dw_numpy,
         pin_i8_pw_numpy, pin_i8_fused_numpy, pin_i8_fused_composition, pin_i8_dense_numpy,
-        pin_i8_pwpw_composition]
+        pin_i8_pwpw_composition, pin_i8_pwdw_numpy, pin_i8_pwdw_composition,
+        pin_i8_pwdw_padding_by_hand]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -299,6 +357,14 @@ MUTANTS = {
         "t += (int64_t)mid[j] * (int64_t)wp[(size_t)j * K + kk];"),
     "dw_i8_pad_sign": ("int hi = ho * s - p + i;\n                        if (hi < 0 || hi >= H) continue;\n                        for (int j = 0; j < k; j++) {\n                            int wi = wo * s - p + j;\n                            if (wi < 0 || wi >= W) continue;\n                            t += (int64_t)",
                        "int hi = ho * s + p + i;\n                        if (hi < 0 || hi >= H) continue;\n                        for (int j = 0; j < k; j++) {\n                            int wi = wo * s - p + j;\n                            if (wi < 0 || wi >= W) continue;\n                            t += (int64_t)"),
+    "pwdw_i8_pads_the_input": (
+        "if (wi < 0 || wi >= W) continue;\n                            int64_t q = 0;\n                            for (int c = 0; c < C; c++)",
+        "int64_t q = 0;\n                            if (wi >= 0 && wi < W) for (int c = 0; c < C; c++)"),
+    "pwdw_i8_wq_transposed": ("(int64_t)wq[(size_t)j * C + c];", "(int64_t)wq[(size_t)c * Cm + j];"),
+    "pwdw_i8_dw_taps_transposed": ("(int64_t)wd2[((size_t)j * k + i) * k + u];",
+                                   "(int64_t)wd2[((size_t)j * k + u) * k + i];"),
+    "pwdw_i8_mid_not_requantized": ("int8_t mval = requant_i8(q, s1[j], b1[j], act1);",
+                                    "int64_t mval = q;"),
 }
 
 

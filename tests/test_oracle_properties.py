@@ -159,3 +159,20 @@ def test_int8_requant_single_values(acc, e, b4, act):
     sc, b = 2.0 ** e, b4 / 4.0
     want = int(requant(np.float64(acc), sc, b, act))
     assert oracle.requant_i8(acc, sc, b, act) == want
+
+
+@settings(**SETTINGS)
+@given(geometry(), st.integers(1, 5), st.integers(1, 6), st.sampled_from(ACTS),
+       st.sampled_from(ACTS), st.integers(0, 2**31 - 1))
+def test_int8_pwdw_matches_library_composition(g, C, Cm, a1, a2, seed):
+    N, H, W, k, s, p = g
+    r = np.random.default_rng(seed)
+    x = r.integers(-128, 128, (N, H, W, C)).astype(np.int8)
+    wq = r.integers(-128, 128, (Cm, C)).astype(np.int8)
+    wd = r.integers(-128, 128, (Cm, k, k)).astype(np.int8)
+    s1, b1 = draw_norm(r, Cm)
+    s2, b2 = draw_norm(r, Cm)
+    mid = requant(t_pw(x, wq), s1.astype(np.float64), b1.astype(np.float64), a1)
+    want = requant(t_dw(mid, wd, s, p), s2.astype(np.float64), b2.astype(np.float64), a2)
+    got = oracle.pwdw_i8(x, wq, s1, b1, wd, s2, b2, a1, a2, s, p)
+    np.testing.assert_array_equal(got, want)
