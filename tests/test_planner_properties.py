@@ -4,11 +4,13 @@ it either returns a plan the kernels can be launched with, or refuses with a sta
 A plan must fit the launch limits of a GB300 (152 SMs, 227 KB of dynamic shared memory a
 block, at most 1024 threads), cover every output pixel with its tiles, and report the byte
 counts of section IV's minimum-traffic reading: input, weights, scale/bias and output once
-fused, plus one write and one read of the intermediate layer by layer.
+fused, plus one write and one read of the intermediate layer by layer.  Its Eq. 1-4 estimates
+for the chosen tile must equal the literal equations (oracle/planner_model.py).
 """
 import pytest
 
 import pointwise_conv_cnn_gb300 as fcm
+from oracle import planner_model as pm
 
 hyp = pytest.importorskip("hypothesis")
 st = hyp.strategies
@@ -160,3 +162,20 @@ def check_plan(kw, info):
     assert info["bytes_fused_min"] == fused
     assert info["bytes_unfused_min"] - fused == 2 * N * mid_px * cm * e
     assert info["overlap_elems"] >= 0 and info["gma_fused_model"] > 0
+
+    # section IV's estimates for the plan's own tile, against the literal equations
+    if kw["conv1"] == "dw":
+        g = pm.layer_pair_gma(H, W, C, K, k, s, p, th, tw)
+        assert info["overlap_elems"] == g["overlap"]
+        assert info["gma_fused_model"] == g["fused"] * N * e
+        assert info["gma_lbl_model"] == g["lbl"] * N * e
+    elif kw["conv1"] == "pwdw":
+        ov = pm.overlap(W, H, tw * s, th * s, k, k, s)
+        wq, wd = cm * C, cm * k * k
+        lbl = (pm.pw_gma(wq, wq, H * W * C, H * W * cm, th * tw * cm)
+               + pm.dw_gma(cm, ov, H * W * cm, ho * wo * cm, ho * wo, th * tw, wd))
+        fused = pm.pwdw_gma(C, ov, H * W * C, wq, wq, wd, wd, ho * wo * cm, th * tw * cm,
+                            ho * wo, th * tw)
+        assert info["overlap_elems"] == ov
+        assert info["gma_lbl_model"] == lbl * N * e
+        assert info["gma_fused_model"] == fused * N * e
