@@ -50,7 +50,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--mode", default="fused", choices=["fused", "unfused"])
-    p.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    p.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "tc_roles", "tc_workers"])
     p.add_argument("--report", default=None, help="write a per-workload JSON report here")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -100,8 +100,21 @@ typedef enum fcm_mode {
 } fcm_mode;
 
 /* Kernel family request.  AUTO picks the tensor-core (tcgen05) kernels whenever the shape
- * is supported by them, else the CUDA-core (SIMT) kernels.  fp32 always runs SIMT. */
-typedef enum fcm_kernel_pref { FCM_KERNEL_AUTO = 0, FCM_KERNEL_SIMT = 1, FCM_KERNEL_TC = 2 } fcm_kernel_pref;
+ * is supported by them, else the CUDA-core (SIMT) kernels.  fp32 always runs SIMT.
+ * The depthwise module has two tensor-core kernels for its fused mode: one with dedicated warp
+ * roles (loader, MMA issuer, epilogue warps, stencil warps) and one whose worker warps each run
+ * the stencil and a share of the 1x1's epilogue.  TC and AUTO take the worker-warp kernel for
+ * 5x5 and 7x7 filters when the shape fits it (C <= 256, 16 <= K <= 256), where it measured
+ * faster, else the role kernel; TC_ROLES and TC_WORKERS ask for one of them (TC_WORKERS fails
+ * with FCM_ERR_UNSUPPORTED where the worker kernel does not take the shape).  Other module
+ * kinds treat both as TC. */
+typedef enum fcm_kernel_pref {
+    FCM_KERNEL_AUTO = 0,
+    FCM_KERNEL_SIMT = 1,
+    FCM_KERNEL_TC = 2,
+    FCM_KERNEL_TC_ROLES = 3,
+    FCM_KERNEL_TC_WORKERS = 4
+} fcm_kernel_pref;
 
 typedef struct fcm_desc {
     int n, h, w, c;        /* input feature maps, NHWC                                     */
@@ -132,6 +145,10 @@ typedef struct fcm_plan_info {
                                     whole batch                                               */
     long long gma_lbl_model;     /* Eq. 3 (DW) + Eq. 2 (PW), bytes, whole batch               */
     long long overlap_elems;     /* Eq. 1 for the chosen tile, elements per channel per image */
+    int tc_variant;              /* depthwise module on tcgen05: 1 = worker-warp kernel (each
+                                    warp runs the stencil and its share of the 1x1's epilogue;
+                                    channels in chunks of 64, the last one zero-padded),
+                                    2 = dedicated warp roles; 0 otherwise                     */
 } fcm_plan_info;
 
 typedef struct fcm_handle fcm_handle;

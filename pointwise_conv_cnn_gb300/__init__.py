@@ -37,7 +37,7 @@ DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3}
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
 CONV1 = {"dw": 0, "dense": 1, "pwdw": 2}
 MODES = {"fused": 0, "conv1": 1, "pw": 2, "unfused": 3}
-KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "tc_roles": 3, "tc_workers": 4}
 
 EXPORTED_SYMBOLS = (
     "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
@@ -65,7 +65,7 @@ class FcmPlanInfo(ctypes.Structure):
         "ho", "wo", "cm", "kernel", "tile_h", "tile_w", "chunk_c", "stages", "ctas", "threads",
         "smem_bytes")] + [(n, ctypes.c_longlong) for n in (
             "num_tiles", "bytes_fused_min", "bytes_unfused_min", "gma_fused_model",
-            "gma_lbl_model", "overlap_elems")]
+            "gma_lbl_model", "overlap_elems")] + [("tc_variant", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

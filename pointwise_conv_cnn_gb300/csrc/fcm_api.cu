@@ -1,4 +1,5 @@
 // fcm_api.cu -- the C ABI: argument checks, handle lifetime, weight repacking, dispatch.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -6,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "fcm_internal.h"
@@ -18,6 +20,33 @@ fcm_status fcm_fail(fcm_status st, const char *fmt, ...) {
     vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
     va_end(ap);
     return st;
+}
+
+unsigned long long fcm_current_ctx_id() {
+    typedef CUresult (*GetCurrentFn)(CUcontext *);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
 }
 
 static fcm_status cuda_fail(cudaError_t e, const char *what) {
@@ -66,7 +95,7 @@ static void free_handle(fcm_handle *h) {
     if (h->ev_start) cudaEventDestroy(h->ev_start);
     if (h->copy_in) cudaStreamDestroy(h->copy_in);
     if (h->copy_out) cudaStreamDestroy(h->copy_out);
-    void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->s1, h->b1,
+    void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->w1dw_pad, h->s1, h->b1,
                     h->s2, h->b2, h->q1, h->i8_one, h->i8_zero, h->i8_idq, h->i8_idtap,
                     h->d_err, h->mid_buf, h->stage_in, h->stage_out};
     for (void *p : ptrs)
@@ -296,7 +325,7 @@ static fcm_handle batch_view(const fcm_handle *h, int nc) {
     v.x_elems = h->x_elems / n * nc;
     v.m_elems = h->m_elems / n * nc;
     v.y_elems = h->y_elems / n * nc;
-    for (TcPlan *p : {&v.tc, &v.tc2}) {
+    for (TcPlan *p : {&v.tc, &v.tc2, &v.tc_lbl}) {
         if (p->num_tiles <= 0) continue;
         p->num_tiles = p->num_tiles / n * nc;
         p->ctas = (int)(p->num_tiles < h->num_sms ? p->num_tiles : h->num_sms);

@@ -32,6 +32,15 @@ struct TcPlan {
     int tmem_cols = 0;
     int out_bufs = 1;             // DW->PW output staging tiles (2: stores overlap the next tile)
     int dw_per_chunk = 0;         // >0: each DW warp serves one channel chunk (taps in registers)
+    // Fused DW->PW kernel variant: 0 = dwpw_kernel (dedicated producer/MMA/epilogue/stencil
+    // warps), 1 = dwpw_fused_kernel (worker warps that run the stencil and the epilogue)
+    int variant = 0;
+    int qw = 0, qh = 0, nqx = 0;  // variant 1: pixels of a TMEM lane quadrant (qw x qh), quadrants across
+    int nw = 0;                   // variant 1: worker warps
+    int abufs = 0;                // variant 1: A tiles (2: the stencil of tile t+1 overlaps the MMA of t)
+    int sbufs = 0;                // variant 1: output staging buffers (2: stores overlap the next tile)
+    int cp = 0;                   // variant 1: channels padded to a multiple of 64
+    int ngroups = 0;              // variant 1: 4-pixel DW units per tile row
 };
 
 struct fcm_handle {
@@ -40,6 +49,8 @@ struct fcm_handle {
     TcPlan tc{};
     TcPlan tc2{};             // PWDW: plan of the layer-by-layer depthwise stage;
                               // INT8: plan of the PW-only stage (identity stencil, k = 1)
+    TcPlan tc_lbl{};          // DW->PW handles whose fused plan is variant 1: the plan of the
+                              // layer-by-layer modes (DW-only, PW-only) on dwpw_kernel
     int device = -1;
     int ho = 0, wo = 0, cm = 0;
     int esize = 0;
@@ -55,6 +66,8 @@ struct fcm_handle {
     void *w1_img = nullptr;   // tcgen05 B-operand images of dense conv1, one per tap
     size_t w1_img_bytes = 0;
     void *w1dw_img = nullptr; // DW taps for the tcgen05 DW stage: [k*k][C], storage dtype (f16 for INT8)
+    void *w1dw_pad = nullptr; // the same taps as [k*k][Cp], Cp = C rounded up to 64, zero-padded
+                              // (dwpw_fused_kernel); INT8 PW-only views point it at i8_idtap
     float *s1 = nullptr, *b1 = nullptr, *s2 = nullptr, *b2 = nullptr;
     // INT8: 1152 * (sum of each channel's taps), and the identity stencil (one f16 tap of 1,
     // scale 1, bias 0, offset 1152) through which the PW-only mode runs on the fused kernel
@@ -76,6 +89,11 @@ struct fcm_handle {
 // thread-local last-error message (fcm_api.cu)
 fcm_status fcm_fail(fcm_status st, const char *fmt, ...);
 
+// Unique id of the calling thread's current CUDA context (never reused within a process), or
+// 0 when there is none or the driver cannot say (fcm_api.cu).  Per-context caches compare it
+// so that they are rebuilt after a device reset or on another device.
+unsigned long long fcm_current_ctx_id();
+
 // planner.cu
 fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm);
 fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm_plan_info *info,
@@ -83,6 +101,15 @@ fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm
 int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);
 fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
                        TcPlan *tc);
+// tc_dwpw.cu: the depthwise -> pointwise plan on dwpw_kernel alone (variant 0), which also
+// serves the layer-by-layer modes
+fcm_status fcm_tc_plan_dwpw_roles(const fcm_desc *d, int ho, int wo, int cm, int num_sms,
+                                  int smem_per_block, TcPlan *tc);
+// tc_dwpw_fused.cu: the depthwise -> pointwise plan on dwpw_fused_kernel (variant 1), or an
+// error status when that kernel does not take the shape or no tile fits
+fcm_status fcm_fused_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, int smem_per_block,
+                          TcPlan *tc);
+cudaError_t launch_tc_fused(const fcm_handle *h, const void *x, void *y, cudaStream_t st);
 
 // tc_b2b.cu: dense k x k -> 1x1 on tcgen05
 int fcm_b2b_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);

@@ -79,7 +79,7 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
     if (d->act1 < FCM_ACT_NONE || d->act1 > FCM_ACT_RELU6 || d->act2 < FCM_ACT_NONE ||
         d->act2 > FCM_ACT_RELU6)
         return fcm_fail(FCM_ERR_INVALID_ARG, "activation code out of range");
-    if (d->kernel < FCM_KERNEL_AUTO || d->kernel > FCM_KERNEL_TC)
+    if (d->kernel < FCM_KERNEL_AUTO || d->kernel > FCM_KERNEL_TC_WORKERS)
         return fcm_fail(FCM_ERR_INVALID_ARG, "kernel preference %d", d->kernel);
     if (d->tile_h < 0 || d->tile_w < 0)
         return fcm_fail(FCM_ERR_INVALID_ARG, "negative tile override");
@@ -171,7 +171,7 @@ fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm
     bool want_tc = d->kernel != FCM_KERNEL_SIMT && d->dtype != FCM_F32;
     bool tc_ok = want_tc && fcm_tc_supported(d, ho, wo, cm, &why) &&
                  fcm_tc_plan(d, ho, wo, cm, num_sms, smem_per_block, t) == FCM_OK;
-    if (d->kernel == FCM_KERNEL_TC && !tc_ok)
+    if (d->kernel >= FCM_KERNEL_TC && !tc_ok)
         return fcm_fail(FCM_ERR_UNSUPPORTED, "tensor-core kernels requested but unavailable: %s",
                         why ? why : (d->dtype == FCM_F32 ? "fp32 runs on CUDA cores" : "no tile fits"));
     if (d->dtype == FCM_I8 && !tc_ok)   // INT8 has no CUDA-core kernels
@@ -180,13 +180,15 @@ fcm_status fcm_make_plan(const fcm_desc *d, int num_sms, int smem_per_block, fcm
     if (tc_ok) {
         info->kernel = FCM_KERNEL_TC;
         info->tile_h = t->tile_h;
-        info->tile_w = t->tile_w;
+        // the worker-warp kernel's tile pitch may exceed the image: report the pixels it covers
+        info->tile_w = t->variant == 1 ? (t->tile_w < wo ? t->tile_w : wo) : t->tile_w;
         info->chunk_c = t->chunk_c;
         info->stages = t->stages;
         info->ctas = t->ctas;
         info->threads = t->threads;
         info->smem_bytes = t->smem_bytes;
         info->num_tiles = t->num_tiles;
+        if (d->conv1 == FCM_CONV1_DEPTHWISE) info->tc_variant = t->variant == 1 ? 1 : 2;
     } else {
         // SIMT kernels: flattened tiles of 32 output pixels, all channels
         const int px = 32;

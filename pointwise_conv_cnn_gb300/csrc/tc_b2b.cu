@@ -97,13 +97,6 @@ struct Bars {
 };
 constexpr uint32_t kBarBytes = 8 * (4 * kMaxStages + 12 + 2) + 16;
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 // 128B-swizzled K-major descriptor whose start may sit at any 128-byte row of a swizzle atom:
 // the tensor core applies the swizzle to absolute shared-memory address bits, the same bits
 // the TMA used when it wrote the tile, so a start shifted by t rows reads pixel i + t as row i

@@ -77,6 +77,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// 16-byte shared-memory load and store by 32-bit shared address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
 // ----------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -368,6 +384,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 // carries into the next one.
 __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
     return d + (uint64_t)(bytes >> 4);
+}
+
+// Byte offset of the 16-wide K step k16 in a K-major operand of `rows` rows stored as 64-wide
+// K blocks of 128-byte swizzled rows.
+__device__ __forceinline__ uint32_t k16_offset(int k16, int rows) {
+    return (uint32_t)(k16 >> 2) * (uint32_t)rows * 128u + (uint32_t)(k16 & 3) * 32u;
 }
 
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands K-major.

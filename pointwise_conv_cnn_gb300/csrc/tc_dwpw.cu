@@ -113,6 +113,18 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
                        TcPlan *p) {
     if (d->conv1 == FCM_CONV1_DENSE) return fcm_b2b_plan(d, ho, wo, cm, num_sms, smem_cap, p);
     if (d->conv1 == FCM_CONV1_POINTWISE) return fcm_pwdw_plan(d, ho, wo, cm, num_sms, smem_cap, p);
+    // the worker-warp kernel where it measured faster (5x5 and 7x7 filters: a long stencil per
+    // unit), or on request; the role kernel otherwise
+    if (d->kernel == FCM_KERNEL_TC_WORKERS)
+        return fcm_fused_plan(d, ho, wo, cm, num_sms, smem_cap, p);
+    if (d->kernel != FCM_KERNEL_TC_ROLES && d->ksize >= 5 &&
+        fcm_fused_plan(d, ho, wo, cm, num_sms, smem_cap, p) == FCM_OK)
+        return FCM_OK;
+    return fcm_tc_plan_dwpw_roles(d, ho, wo, cm, num_sms, smem_cap, p);
+}
+
+fcm_status fcm_tc_plan_dwpw_roles(const fcm_desc *d, int ho, int wo, int cm, int num_sms,
+                                  int smem_cap, TcPlan *p) {
     const int S = d->stride, KS = d->ksize, C = cm;
     TcPlan best;
     double best_score = -1.0;
@@ -233,7 +245,11 @@ fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
         }
     }
     const __half h1 = __float2half_rn(1.0f);
-    std::vector<__half> idtap(C, h1);
+    // the identity taps, zero-padded to a multiple of 64 channels (the worker-warp kernel
+    // reads [k*k][Cp] taps)
+    const int cp = (C + 63) / 64 * 64;
+    std::vector<__half> idtap(cp, __float2half_rn(0.0f));
+    for (int c = 0; c < C; c++) idtap[c] = h1;
     const size_t fb = (size_t)C * sizeof(float);
     if (cudaMalloc(&h->q1, fb) != cudaSuccess ||
         cudaMemcpy(h->q1, q1.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -243,8 +259,8 @@ fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
         cudaMemcpy(h->i8_zero, zero.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMalloc(&h->i8_idq, fb) != cudaSuccess ||
         cudaMemcpy(h->i8_idq, idq.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMalloc(&h->i8_idtap, (size_t)C * 2) != cudaSuccess ||
-        cudaMemcpy(h->i8_idtap, idtap.data(), (size_t)C * 2, cudaMemcpyHostToDevice) != cudaSuccess)
+        cudaMalloc(&h->i8_idtap, (size_t)cp * 2) != cudaSuccess ||
+        cudaMemcpy(h->i8_idtap, idtap.data(), (size_t)cp * 2, cudaMemcpyHostToDevice) != cudaSuccess)
         return fcm_fail(FCM_ERR_CUDA, "INT8 stencil constants: %s",
                         cudaGetErrorString(cudaGetLastError()));
     const fcm_desc v = i8_pw_desc(h);
@@ -288,12 +304,24 @@ fcm_status fcm_tc_prepare(fcm_handle *h, const void *w1_host, const void *wp_hos
         fcm_status st = fcm_i8_prepare(h, w1_host);
         if (st != FCM_OK) return st;
     }
+    // the same taps with the channel stride padded to a multiple of 64 (worker-warp kernel)
+    const int cp = nkb * 64;
+    std::vector<uint16_t> wdwp((size_t)cp * KS * KS, 0);
+    for (int t = 0; t < KS * KS; t++)
+        for (int c = 0; c < C; c++) wdwp[(size_t)t * cp + c] = wdw[(size_t)t * C + c];
     if (cudaMalloc(&h->wp_img, h->wp_img_bytes) != cudaSuccess ||
         cudaMemcpy(h->wp_img, img.data(), h->wp_img_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMalloc(&h->w1dw_img, wdw.size() * 2) != cudaSuccess ||
-        cudaMemcpy(h->w1dw_img, wdw.data(), wdw.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess)
+        cudaMemcpy(h->w1dw_img, wdw.data(), wdw.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->w1dw_pad, wdwp.size() * 2) != cudaSuccess ||
+        cudaMemcpy(h->w1dw_pad, wdwp.data(), wdwp.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess)
         return fcm_fail(FCM_ERR_CUDA, "tensor-core weight images: %s",
                         cudaGetErrorString(cudaGetLastError()));
+    // the layer-by-layer modes run on dwpw_kernel: their own plan when the fused mode runs on
+    // the worker-warp kernel
+    if (h->tc.variant == 1 &&
+        fcm_tc_plan_dwpw_roles(&h->d, h->ho, h->wo, C, h->num_sms, h->smem_optin, &h->tc_lbl) != FCM_OK)
+        return fcm_fail(FCM_ERR_SMEM_BUDGET, "layer-by-layer DW->PW stages: no tile fits");
     return FCM_OK;
 }
 
@@ -320,8 +348,9 @@ cudaError_t dispatch_ks(const Args &a, int ks, int s, int ctas, int threads, uin
 }
 
 cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out, cudaStream_t st) {
+    if (mode == FUSED && h->tc.variant == 1) return launch_tc_fused(h, in, out, st);
     const fcm_desc &d = h->d;
-    const TcPlan &p = h->tc;
+    const TcPlan &p = h->tc.variant == 1 ? h->tc_lbl : h->tc;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int out_bufs = mode == FUSED ? p.out_bufs : 1;
@@ -456,6 +485,7 @@ cudaError_t launch_tc_pw(const fcm_handle *h, const void *m, void *y, cudaStream
         v.b1 = h->i8_zero;
         v.q1 = h->i8_idq;
         v.w1dw_img = h->i8_idtap;
+        v.w1dw_pad = h->i8_idtap;
         return launch_mode(&v, FUSED, m, y, st);
     }
     return launch_mode(h, PWONLY, m, y, st);

@@ -1,0 +1,15 @@
+// tc_dwpw_fused_inst_bf16_k13.cu -- instantiations of the worker-warp DW->PW kernel for bfloat16
+// storage and filter sizes 1 and 3 (one of several translation units, compiled in parallel).
+#define FCM_FUSED_KERNEL_BODY
+#include "tc_dwpw_fused.cuh"
+
+namespace fcm {
+namespace tc {
+
+template cudaError_t launch_fused<__nv_bfloat16, 1, 1>(const FArgs &, int, int, uint32_t, cudaStream_t);
+template cudaError_t launch_fused<__nv_bfloat16, 1, 2>(const FArgs &, int, int, uint32_t, cudaStream_t);
+template cudaError_t launch_fused<__nv_bfloat16, 3, 1>(const FArgs &, int, int, uint32_t, cudaStream_t);
+template cudaError_t launch_fused<__nv_bfloat16, 3, 2>(const FArgs &, int, int, uint32_t, cudaStream_t);
+
+}  // namespace tc
+}  // namespace fcm

@@ -37,21 +37,6 @@
 namespace fcm {
 namespace tc {
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 // Where one DW work unit (kR consecutive output pixels of one tile row, 8 channels) sits in a
 // stage and in the A tile.  None of it depends on the tile or on the channel chunk, so each
 // thread works it out once for the units it owns.
@@ -190,12 +175,6 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
             }
         }
     }
-}
-
-// Byte offset of the 16-wide K step k16 in a K-major operand of `rows` rows stored as 64-wide
-// K blocks of 128-byte swizzled rows.
-__device__ __forceinline__ uint32_t k16_offset(int k16, int rows) {
-    return (uint32_t)(k16 >> 2) * (uint32_t)rows * 128u + (uint32_t)(k16 & 3) * 32u;
 }
 
 __device__ __forceinline__ void tile_coords(const Args &a, int t, int &n, int &ho0, int &wo0) {
@@ -403,6 +382,9 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const bool issuer = warp == 2 && lane == 0;
+        // kEpiWarps / 4 warps per TMEM lane quadrant split the columns in groups of 16
+        const int ng = a.K / 16, part = (warp - 2) >> 2, nparts = kEpiWarps / 4;
+        const int c_lo = (part * ng / nparts) * 16, c_hi = ((part + 1) * ng / nparts) * 16;
         const int nkb_out = (a.K + 63) / 64;
         const uint32_t swz = kI8 ? (uint32_t)((row >> 1) & 3) : (uint32_t)(row & 7);
         uint32_t out_s = base_s + a.off_out, row_s = out_s + (uint32_t)row * kRowBytes;
@@ -466,9 +448,9 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
                 // two loads of 16 columns, one wait (K is a multiple of 16; keeping a load in
                 // flight across the conversion measured slower)
-                for (int c0 = 0; c0 < a.K; c0 += 32) {
+                for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                     uint32_t ra[16], rb[16];
-                    const bool two = c0 + 16 < a.K;
+                    const bool two = c0 + 16 < c_hi;
                     tmem_ld16(taddr + (uint32_t)c0, ra);
                     if (two) tmem_ld16(taddr + (uint32_t)(c0 + 16), rb);
                     tmem_ld_wait();
@@ -511,8 +493,8 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
             const int tid = (dw_w % a.dw_per_chunk) * 32 + lane;
             const bool has_unit = tid < units;
             const DwUnit g0 = dw_unit_geom<T, S>(a, has_unit ? tid : 0);
-            uint4 wreg[KS * KS];
-            {
+            uint4 wreg[KS * KS] = {};
+            if (kDwTapsInRegs) {
                 const uint8_t *wb = wdw_g + (uint32_t)(jm * a.chunk_c + g0.cv) * 2u;
 #pragma unroll
                 for (int t = 0; t < KS * KS; t++)
@@ -533,7 +515,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                         break;
                     const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
                     if (has_unit)
-                        dw_unit<T, KS, S, MODE, ACT, true>(a, g0, jm, stage_g, wdw_g, wreg, s1_s,
+                        dw_unit<T, KS, S, MODE, ACT, kDwTapsInRegs>(a, g0, jm, stage_g, wdw_g, wreg, s1_s,
                                                            b1_s, q1_s, a_s, n, ho0, wo0);
                     if (MODE == FUSED) fence_proxy_async_smem();
                     __syncwarp();

@@ -78,13 +78,6 @@ struct Bars {
 };
 constexpr uint32_t kBarBytes = 8 * (2 * kMaxStages + 8 + 2) + 16;
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tile_coords(const Args &a, int t, int &n, int &ho0) {
     n = t / a.tiles_per_img;
     ho0 = (t - n * a.tiles_per_img) * a.TH;
@@ -572,7 +565,7 @@ fcm_status fcm_pwdw_prepare(fcm_handle *h, const void *w1_host, const void *wp_h
     dd.mid = 0;
     dd.k_out = 16;   // the DW-only mode has no 1x1 stage: plan with the smallest one
     dd.tile_h = dd.tile_w = 0;
-    fcm_status st = fcm_tc_plan(&dd, h->ho, h->wo, Cm, h->num_sms, h->smem_optin, &h->tc2);
+    fcm_status st = fcm_tc_plan_dwpw_roles(&dd, h->ho, h->wo, Cm, h->num_sms, h->smem_optin, &h->tc2);
     if (st != FCM_OK) return fcm_fail(st, "PWDW: no tile for the layer-by-layer depthwise stage");
     return FCM_OK;
 }

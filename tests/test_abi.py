@@ -47,7 +47,7 @@ def test_desc_struct_matches_header():
     names = [n for decl in body.split(";") for n in re.findall(r"(\w+)\s*(?:,|$)", decl.replace("int", "", 1).strip())]
     assert [f for f, _ in fcm.FcmDesc._fields_] == names
     assert ctypes.sizeof(fcm.FcmDesc) == 16 * 4
-    assert ctypes.sizeof(fcm.FcmPlanInfo) == 11 * 4 + 4 + 6 * 8
+    assert ctypes.sizeof(fcm.FcmPlanInfo) == 11 * 4 + 4 + 6 * 8 + 8   # tc_variant + tail padding
 
 
 def good_desc(**kw):

@@ -14,7 +14,10 @@ from helpers import (assert_bitexact, assert_parity, empty, make_module, oracle_
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["simt", "tc"]
+# the depthwise module's two tensor-core kernels: "tc_roles" (dedicated warp roles) and
+# "tc_workers" (worker warps running the stencil and the epilogue); for the other modules both
+# mean "tc"
+KERNELS = ["simt", "tc_roles", "tc_workers"]
 
 
 def reduced(wl: wk.Workload, n=2, hw=None) -> wk.Workload:
@@ -27,6 +30,8 @@ def reduced(wl: wk.Workload, n=2, hw=None) -> wk.Workload:
 
 
 def module_or_skip(case, kernel):
+    if kernel == "tc_workers" and case.wl.conv1 != "dw":
+        pytest.skip("only the depthwise module has a second tensor-core kernel")
     if case.wl.dtype == "i8" and kernel == "simt":
         # INT8 has no CUDA-core kernels: the request is refused, not served by another path
         with pytest.raises(fcm.FcmError) as e:
@@ -36,7 +41,7 @@ def module_or_skip(case, kernel):
     try:
         return make_module(case, kernel)
     except fcm.FcmError as e:
-        if kernel == "tc" and e.status == 2:
+        if kernel in ("tc", "tc_roles", "tc_workers") and e.status == 2:
             pytest.skip(f"tensor-core kernels do not take this shape: {e}")
         raise
 
@@ -106,6 +111,12 @@ EDGE = [  # (N, H, W, C, K, k, s, p, dtype, act1, act2)
     (1, 20, 131, 16, 16, 3, 1, 1, "f16", "relu", "relu"),
     (1, 15, 15, 8, 8, 3, 2, 0, "f32", "relu", "relu"),
     (2, 6, 9, 12, 20, 5, 1, 2, "f32", "relu6", "relu6"),
+    # channel counts that leave the last 64-channel chunk partly empty, 3 and 4 chunks,
+    # quadrants of 16 x 2 pixels, several tiles across, K = 256 with stride 2
+    (2, 14, 14, 96, 64, 3, 1, 1, "f16", "relu6", "relu6"),
+    (1, 33, 33, 192, 80, 5, 1, 2, "bf16", "relu", "none"),
+    (2, 9, 70, 256, 256, 3, 2, 1, "f16", "none", "relu"),
+    (1, 5, 9, 240, 80, 5, 1, 2, "bf16", "relu", "none"),
 ]
 
 
@@ -114,7 +125,7 @@ EDGE = [  # (N, H, W, C, K, k, s, p, dtype, act1, act2)
 def test_edge_shapes(cuda, shape, kernel):
     N, H, W, C, K, k, s, p, dt, a1, a2 = shape
     wl = wk.Workload("edge", N, H, W, C, K, "dw", k, s, p, a1, a2, dt, "normal")
-    if kernel == "tc" and dt == "f32":
+    if kernel in ("tc", "tc_roles", "tc_workers") and dt == "f32":
         pytest.skip("fp32 runs on CUDA cores")
     case = wk.make_case(wl, seed=77)
     mod = module_or_skip(case, kernel)
@@ -181,7 +192,7 @@ def test_pwdw_edge_shapes(cuda, shape, kernel):
     kind = "integer" if wk.integer_safe(wl) else "integer1"
     if wk.integer_safe(wl, kind):
         icase = wk.make_case(wl, seed=8, kind=kind)
-        imod = make_module(icase, kernel) if kernel != "tc" else module_or_skip(icase, kernel)
+        imod = make_module(icase, kernel) if kernel == "simt" else module_or_skip(icase, kernel)
         iref = oracle_fused(icase)
         for mode in ("fused", "unfused"):
             got, _ = run_case(icase, mode, module=imod)
@@ -200,8 +211,9 @@ I8_EDGE = [  # (N, H, W, C, K, k, s, p, act1, act2): the INT8 module, int8 over 
 ]
 
 
+@pytest.mark.parametrize("kernel", ["tc_roles", "tc_workers"])
 @pytest.mark.parametrize("shape", I8_EDGE, ids=lambda s: "x".join(map(str, s[:8])))
-def test_int8_edge_shapes(cuda, shape):
+def test_int8_edge_shapes(cuda, shape, kernel):
     """INT8 DW -> PW: bit-exact with the oracle in every mode (fused, layer by layer, the
     depthwise layer alone, the 1x1 on the oracle's intermediate): ragged tiles, 1x1 images,
     stride 2, k = 1, 5, 7, the widest channel counts."""
@@ -209,7 +221,7 @@ def test_int8_edge_shapes(cuda, shape):
     N, H, W, C, K, k, s, p, a1, a2 = shape
     wl = wk.Workload("i8_edge", N, H, W, C, K, "dw", k, s, p, a1, a2, "i8", "int8")
     case = wk.make_case(wl, seed=91)
-    mod = make_module(case, "tc")
+    mod = make_module(case, kernel)
     ref = oracle_fused(case)
     for mode in ("fused", "unfused"):
         got, _ = run_case(case, mode, module=mod)

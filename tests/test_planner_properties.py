@@ -147,7 +147,11 @@ def check_plan(kw, info):
         # coordinate times the element size must be a multiple of 16 bytes
         assert info["chunk_c"] > 0 and (info["chunk_c"] * ESIZE[kw["dtype"]]) % 16 == 0
         if kw["conv1"] == "dw":
-            assert th * tw <= 128 and cm % info["chunk_c"] == 0
+            assert th * tw <= 128
+            if info["tc_variant"] == 1:   # worker-warp kernel: 64-channel chunks, last one padded
+                assert info["chunk_c"] == 64 and cm <= 256
+            else:
+                assert info["tc_variant"] == 2 and cm % info["chunk_c"] == 0
     else:
         assert 0 < info["ctas"] <= min(info["num_tiles"], 8 * NUM_SMS)
         # flattened tiles of 32 output pixels (tile_w reports min(32, Wo) for the cost models)
