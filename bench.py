@@ -158,7 +158,7 @@ def oracle_step(oracle, wk, wl, case, nthreads: int):
     """One evaluation of the oracle's single-pass module on `case` (fp64, or the INT8 one) with
     `nthreads` OpenMP threads (the oracle's thread count is sticky, so every call sets it)."""
     if wl.dtype == "i8":
-        fn = oracle.fused_dense_i8 if wl.conv1 == "dense" else oracle.fused_i8
+        fn = {"dense": oracle.fused_dense_i8, "pwdw": oracle.pwdw_i8}.get(wl.conv1, oracle.fused_i8)
         return lambda: fn(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2, wl.act1,
                           wl.act2, wl.stride, wl.pad, nthreads=nthreads)
     f = case.f64()

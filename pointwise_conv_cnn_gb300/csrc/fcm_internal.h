@@ -50,7 +50,8 @@ struct fcm_handle {
     TcPlan tc2{};             // PWDW: plan of the layer-by-layer depthwise stage;
                               // INT8: plan of the PW-only stage (identity stencil, k = 1)
     TcPlan tc_lbl{};          // DW->PW handles whose fused plan is variant 1: the plan of the
-                              // layer-by-layer modes (DW-only, PW-only) on dwpw_kernel
+                              // layer-by-layer modes (DW-only, PW-only) on dwpw_kernel;
+                              // INT8 PWDW: the plan of its first layer alone (identity stencil)
     int device = -1;
     int ho = 0, wo = 0, cm = 0;
     int esize = 0;
@@ -120,6 +121,8 @@ fcm_status fcm_b2b_prepare(fcm_handle *h, const void *w1_host, const void *wp_ho
 // tc_dwpw.cu: INT8 parts of a handle (stencil offsets of a depthwise w1_host, or none when
 // w1_host is NULL; the identity stencil and plan of the PW-only mode)
 fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host);
+fcm_status fcm_i8_constants(fcm_handle *h, const void *taps_host, int n_id);
+fcm_desc fcm_i8_pw_desc(const fcm_handle *h);
 
 // tc_pwdw.cu: 1x1 -> depthwise (PWDW) on tcgen05 + CUDA cores
 int fcm_pwdw_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why);

@@ -73,9 +73,6 @@ fcm_status fcm_validate_desc(const fcm_desc *d, int *ho, int *wo, int *cm) {
         return fcm_fail(FCM_ERR_INVALID_ARG, "conv1 kind %d", d->conv1);
     if (d->dtype < FCM_F32 || d->dtype > FCM_I8)
         return fcm_fail(FCM_ERR_INVALID_ARG, "dtype %d", d->dtype);
-    if (d->dtype == FCM_I8 && d->conv1 == FCM_CONV1_POINTWISE)
-        return fcm_fail(FCM_ERR_UNSUPPORTED,
-                        "INT8 runs the depthwise -> pointwise and the 1x1 -> 1x1 modules");
     if (d->act1 < FCM_ACT_NONE || d->act1 > FCM_ACT_RELU6 || d->act2 < FCM_ACT_NONE ||
         d->act2 > FCM_ACT_RELU6)
         return fcm_fail(FCM_ERR_INVALID_ARG, "activation code out of range");

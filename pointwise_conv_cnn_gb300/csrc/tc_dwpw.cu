@@ -208,11 +208,9 @@ fcm_status fcm_tc_plan_dwpw_roles(const fcm_desc *d, int ho, int wo, int cm, int
     return FCM_OK;
 }
 
-namespace {
-
 // The PW-only mode of an INT8 handle: the fused DW->PW kernel with an identity stencil over the
 // intermediate m [N, Ho, Wo, Cm].
-fcm_desc i8_pw_desc(const fcm_handle *h) {
+fcm_desc fcm_i8_pw_desc(const fcm_handle *h) {
     fcm_desc v = h->d;
     v.conv1 = FCM_CONV1_DEPTHWISE;   // the identity stencil (also for the PWPW module's 2nd layer)
     v.h = h->ho;
@@ -228,14 +226,15 @@ fcm_desc i8_pw_desc(const fcm_handle *h) {
     return v;
 }
 
-}  // namespace
-
-// INT8 handle parts: the per-channel stencil offsets 1152 * sum(taps) (depthwise module only,
-// w1_host = its taps), the identity stencil of the PW-only mode and that mode's plan (the fused
-// DW->PW kernel with k = 1 over the intermediate).
-fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
+// INT8 constants of a handle: the per-channel stencil offsets 1152 * sum(taps) of the h->cm
+// channels of a depthwise layer (taps_host [cm][k][k], or none), and the identity stencil
+// (one f16 tap of 1, scale 1, bias 0, offset 1152) over n_id channels, through which the fused
+// DW->PW kernel runs a lone 1x1 convolution.
+fcm_status fcm_i8_constants(fcm_handle *h, const void *taps_host, int n_id) {
     const int C = h->cm, KS = h->d.ksize;
-    std::vector<float> q1(C, 0.0f), one(C, 1.0f), zero(C, 0.0f), idq(C, I8::kBias);
+    const int ni = std::max(n_id, C);
+    std::vector<float> q1(C, 0.0f), one(ni, 1.0f), zero(ni, 0.0f), idq(ni, I8::kBias);
+    const void *w1_host = taps_host;
     if (w1_host) {
         const signed char *w8 = static_cast<const signed char *>(w1_host);
         for (int c = 0; c < C; c++) {
@@ -247,23 +246,33 @@ fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
     const __half h1 = __float2half_rn(1.0f);
     // the identity taps, zero-padded to a multiple of 64 channels (the worker-warp kernel
     // reads [k*k][Cp] taps)
-    const int cp = (C + 63) / 64 * 64;
+    const int cp = (ni + 63) / 64 * 64;
     std::vector<__half> idtap(cp, __float2half_rn(0.0f));
-    for (int c = 0; c < C; c++) idtap[c] = h1;
-    const size_t fb = (size_t)C * sizeof(float);
+    for (int c = 0; c < ni; c++) idtap[c] = h1;
+    const size_t fb = (size_t)C * sizeof(float), fbi = (size_t)ni * sizeof(float);
     if (cudaMalloc(&h->q1, fb) != cudaSuccess ||
         cudaMemcpy(h->q1, q1.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMalloc(&h->i8_one, fb) != cudaSuccess ||
-        cudaMemcpy(h->i8_one, one.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMalloc(&h->i8_zero, fb) != cudaSuccess ||
-        cudaMemcpy(h->i8_zero, zero.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMalloc(&h->i8_idq, fb) != cudaSuccess ||
-        cudaMemcpy(h->i8_idq, idq.data(), fb, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_one, fbi) != cudaSuccess ||
+        cudaMemcpy(h->i8_one, one.data(), fbi, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_zero, fbi) != cudaSuccess ||
+        cudaMemcpy(h->i8_zero, zero.data(), fbi, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMalloc(&h->i8_idq, fbi) != cudaSuccess ||
+        cudaMemcpy(h->i8_idq, idq.data(), fbi, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMalloc(&h->i8_idtap, (size_t)cp * 2) != cudaSuccess ||
         cudaMemcpy(h->i8_idtap, idtap.data(), (size_t)cp * 2, cudaMemcpyHostToDevice) != cudaSuccess)
         return fcm_fail(FCM_ERR_CUDA, "INT8 stencil constants: %s",
                         cudaGetErrorString(cudaGetLastError()));
-    const fcm_desc v = i8_pw_desc(h);
+    return FCM_OK;
+}
+
+// INT8 handle parts of the depthwise and PWPW modules: the constants above (w1_host = the
+// depthwise taps, or none) and the plan of the PW-only mode (the fused DW->PW kernel with
+// k = 1 over the intermediate).
+fcm_status fcm_i8_prepare(fcm_handle *h, const void *w1_host) {
+    fcm_status st = fcm_i8_constants(h, w1_host, h->cm);
+    if (st != FCM_OK) return st;
+    const int C = h->cm;
+    const fcm_desc v = fcm_i8_pw_desc(h);
     if (fcm_tc_plan(&v, h->ho, h->wo, C, h->num_sms, h->smem_optin, &h->tc2) != FCM_OK)
         return fcm_fail(FCM_ERR_SMEM_BUDGET, "INT8 PW-only stage: no tile fits");
     return FCM_OK;
@@ -479,7 +488,7 @@ cudaError_t launch_tc_pw(const fcm_handle *h, const void *m, void *y, cudaStream
         // INT8: the fused kernel over m with the identity stencil (k = 1, tap 1, scale 1,
         // bias 0, no activation), which hands each int8 value of m to the tensor core as f16
         fcm_handle v = *h;
-        v.d = i8_pw_desc(h);
+        v.d = fcm_i8_pw_desc(h);
         v.tc = h->tc2;
         v.s1 = h->i8_one;
         v.b1 = h->i8_zero;

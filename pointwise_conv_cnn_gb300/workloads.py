@@ -226,6 +226,10 @@ WORKLOADS = (
     # the PWPW pair in INT8: 1x1 64 -> 128 (ReLU), 1x1 128 -> 64 (none)
     Workload("pwpw_i8", 64, 56, 56, 64, 64, "dense", 1, 1, 0, "relu", "none", "i8", "int8",
              mid=128),
+    # the PWDW pair in INT8: 1x1 64 -> 192 (ReLU), then depthwise 3x3 s1 over the 192 channels
+    # (ReLU)
+    Workload("pwdw_i8", 64, 56, 56, 64, 192, "pwdw", 3, 1, 1, "relu", "relu", "i8", "int8",
+             mid=192),
 )
 BY_NAME = {w.name: w for w in WORKLOADS}
 

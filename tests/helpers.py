@@ -73,7 +73,7 @@ def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
 def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.ndarray:
     wl = case.wl
     if wl.dtype == "i8":   # int8 results, as float64 for the shared comparisons
-        fn = oracle.fused_dense_i8 if wl.conv1 == "dense" else oracle.fused_i8
+        fn = {"dense": oracle.fused_dense_i8, "pwdw": oracle.pwdw_i8}.get(wl.conv1, oracle.fused_i8)
         return fn(case.x, case.w1, case.s1, case.b1, case.wp, case.s2, case.b2, wl.act1, wl.act2,
                   wl.stride, wl.pad, nthreads=nthreads).astype(np.float64)
     f = case.f64()
@@ -87,6 +87,8 @@ def oracle_fused(case: wk.Case, mid: str = "exact", nthreads: int = 0) -> np.nda
 def oracle_conv1(case: wk.Case) -> np.ndarray:
     wl = case.wl
     if wl.dtype == "i8":
+        if wl.conv1 == "pwdw":   # the 1x1 layer, over the input's extent
+            return oracle.pw_i8(case.x, case.w1, case.s1, case.b1, wl.act1).astype(np.float64)
         fn = oracle.dense_i8 if wl.conv1 == "dense" else oracle.dw_i8
         return fn(case.x, case.w1, case.s1, case.b1, wl.act1, wl.stride, wl.pad).astype(np.float64)
     f = case.f64()
@@ -101,6 +103,9 @@ def oracle_pw(case: wk.Case, m: np.ndarray) -> np.ndarray:
     """The module's second convolution on an intermediate (the depthwise one for PWDW)."""
     wl = case.wl
     if wl.dtype == "i8":
+        if wl.conv1 == "pwdw":   # the depthwise layer over the intermediate
+            return oracle.dw_i8(np.asarray(m).astype(np.int8), case.wp, case.s2, case.b2, wl.act2,
+                                wl.stride, wl.pad).astype(np.float64)
         return oracle.pw_i8(np.asarray(m).astype(np.int8), case.wp, case.s2, case.b2,
                             wl.act2).astype(np.float64)
     f = case.f64()

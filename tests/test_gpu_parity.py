@@ -236,8 +236,45 @@ def test_int8_edge_shapes(cuda, shape, kernel):
     assert_bitexact(to_host(y, "i8"), oracle_pw(case, m_ref), "i8")
 
 
+PWDW_I8_EDGE = [  # (N, H, W, C, Cm, k, s, p, act1, act2): the INT8 PWDW module
+    (2, 9, 13, 64, 64, 3, 1, 1, "relu", "none"),
+    (1, 11, 60, 64, 128, 3, 2, 1, "relu", "relu"),
+    (3, 7, 20, 128, 64, 5, 1, 2, "none", "relu"),
+    (2, 6, 6, 64, 192, 1, 1, 0, "relu", "none"),
+    (1, 13, 17, 64, 128, 7, 1, 3, "relu6", "none"),
+    (1, 9, 9, 256, 64, 3, 1, 1, "relu", "relu"),
+]
+
+
+@pytest.mark.parametrize("shape", PWDW_I8_EDGE, ids=lambda s: "x".join(map(str, s[:8])))
+def test_int8_pwdw_edge_shapes(cuda, shape):
+    """INT8 1x1 -> depthwise: bit-exact with the oracle fused (the int8 intermediate recomputed
+    under every depthwise tap, int8 zero in the padding), layer by layer, the 1x1 layer alone,
+    and the depthwise layer on the oracle's intermediate; halos across the image border, stride
+    2, k = 1, 5, 7, and C = 256 (the 1x1's widest exact reduction; with a 3x3 halo, since a
+    7x7 one of 256 channels does not fit shared memory)."""
+    import torch
+    N, H, W, C, Cm, k, s, p, a1, a2 = shape
+    wl = wk.Workload("i8_pwdw", N, H, W, C, Cm, "pwdw", k, s, p, a1, a2, "i8", "int8", mid=Cm)
+    case = wk.make_case(wl, seed=95)
+    mod = make_module(case, "tc")
+    ref = oracle_fused(case)
+    for mode in ("fused", "unfused"):
+        got, _ = run_case(case, mode, module=mod)
+        assert_bitexact(got, ref, "i8")
+    m_ref = oracle_conv1(case)
+    m_gpu, _ = run_case(case, "conv1", module=mod)
+    assert_bitexact(m_gpu, m_ref, "i8")
+    y = empty(wl.shapes()["y"], "i8", fill=float("nan"))
+    mod.run(to_device(m_ref.astype(np.int8), "i8"), y, "pw")
+    torch.cuda.synchronize()
+    mod.check()
+    assert_bitexact(to_host(y, "i8"), oracle_pw(case, m_ref), "i8")
+
+
 def test_int8_shapes_refused(cuda):
-    """INT8 requests outside the tensor-core kernels fail with FCM_ERR_UNSUPPORTED."""
+    """INT8 requests outside the tensor-core kernels fail with FCM_ERR_UNSUPPORTED (a dense
+    3x3 first layer, more than 256 channels, a PWDW input that is not a multiple of 64)."""
     for kw in ({"conv1": "dense", "mid": 32}, {"c": 512, "k_out": 64},
                {"conv1": "pwdw", "mid": 32}):
         wl = wk.Workload("i8_no", 1, 8, 8, kw.get("c", 32), kw.get("k_out", 32),

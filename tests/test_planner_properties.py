@@ -50,8 +50,6 @@ def expected_refusal(kw):
     """Requests the planner must refuse whatever the tile search finds, with their status."""
     e = ESIZE[kw["dtype"]]
     cm = kw["mid"] or kw["c"]
-    if kw["dtype"] == "i8" and kw["conv1"] == "pwdw":
-        return 2                                     # no INT8 PWDW module (checked first)
     if any((v * e) % 16 for v in (kw["c"], cm, kw["k_out"])):
         return 3                                     # FCM_ERR_ALIGNMENT
     if kw["dtype"] == "i8" and kw["kernel"] == "simt":
