@@ -263,6 +263,8 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
     "integer" -> small integers (x in [-3,3], weights in [-2,2]) chosen so that every partial
     sum is exact in fp32 and the intermediate is exact in the storage format (bit-exact
     checks); "integer1" -> the same with x and weights in [-1,1], for wide dense layers;
+    "integer_pow2" / "integer1_pow2" -> the same with scales 1/2, 1 or 2 per channel (exact in
+    every format, so that the scale of each channel is checked bit for bit too);
     "int8" -> int8 activations and weights uniform over [-128, 127] with fp32 requantization
     scales that put the intermediate's and the output's spread near 32 (their tails saturate)
     and biases uniform in [-4, 4] (int8 units)."""
@@ -272,13 +274,17 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
     cnt = {name: int(np.prod(sh[name])) for name in _TID}
     fan1, fan2 = wl.fan_in()
     d = wl.dtype
-    if kind in ("integer", "integer1"):
-        xr, wr = (3, 2) if kind == "integer" else (1, 1)
+    if kind in ("integer", "integer1", "integer_pow2", "integer1_pow2"):
+        xr, wr = (3, 2) if kind.startswith("integer_") or kind == "integer" else (1, 1)
         x = integers(seed, _TID["x"], cnt["x"], -xr, xr)
         w1 = integers(seed, _TID["w1"], cnt["w1"], -wr, wr)
         wp = integers(seed, _TID["wp"], cnt["wp"], -wr, wr)
-        s1 = np.ones(cnt["s1"])
-        s2 = np.ones(cnt["s2"])
+        if kind.endswith("_pow2"):
+            s1 = np.exp2(integers(seed, _TID["s1"], cnt["s1"], -1, 1))
+            s2 = np.exp2(integers(seed, _TID["s2"], cnt["s2"], -1, 1))
+        else:
+            s1 = np.ones(cnt["s1"])
+            s2 = np.ones(cnt["s2"])
         b1 = integers(seed, _TID["b1"], cnt["b1"], -2, 2)
         b2 = integers(seed, _TID["b2"], cnt["b2"], -2, 2)
     else:
@@ -313,6 +319,12 @@ def make_case(wl: Workload, seed: int | None = None, kind: str | None = None) ->
                 f32(s2, "s2"), f32(b2, "b2"))
 
 
+# largest magnitude up to which a format holds every integer (the "_half" entries: every
+# multiple of 1/2)
+_EXACT_LIM = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8, "f16_half": 1 << 10,
+              "bf16_half": 1 << 7}
+
+
 def integer_safe(wl: Workload, kind: str = "integer") -> bool:
     """True when the integer case of `wl` is exact end to end: fp32 partial sums stay below
     2^24 and the intermediate (|m| <= k*k*max|x*w| + 2, before the activation) is exactly
@@ -320,14 +332,19 @@ def integer_safe(wl: Workload, kind: str = "integer") -> bool:
     if wl.dtype == "i8":
         return True   # int8 arithmetic is exact integer arithmetic at every size
     k = wl.ksize
-    prod = 6 if kind == "integer" else 1
+    prod = 6 if kind in ("integer", "integer_pow2") else 1
+    if kind.endswith("_pow2"):
+        # scales up to 2 double the values, scales of 1/2 need one bit below the integers: check
+        # the doubled sums against half the format's exact range
+        prod *= 2
+        wl = wl.with_(dtype={"f16": "f16_half", "bf16": "bf16_half"}.get(wl.dtype, wl.dtype))
     if wl.conv1 == "pwdw":
         # the 1x1 sum over C, then k*k depthwise products of the intermediate
         per1 = wl.c * prod + 2
-        lim = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8}[wl.dtype]
+        lim = _EXACT_LIM[wl.dtype]
         mid_max = min(per1, 6) if wl.act1 == "relu6" else per1
         return per1 <= lim and k * k * mid_max * (prod // 3 + 1) + 2 < (1 << 24)
     per1 = k * k * (wl.c if wl.conv1 == "dense" else 1) * prod + 2
-    lim = {"f32": 1 << 24, "f16": 1 << 11, "bf16": 1 << 8}[wl.dtype]
+    lim = _EXACT_LIM[wl.dtype]
     mid_max = min(per1, 6) if wl.act1 == "relu6" else per1
     return per1 < (1 << 24) and mid_max <= lim and wl.cm * mid_max * (prod // 3 + 1) + 2 < (1 << 24)

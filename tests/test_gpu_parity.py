@@ -72,6 +72,65 @@ def test_integer_bitexact_fused_and_unfused(cuda, wl, kernel):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_integer_pow2_scales_bitexact(cuda, wl, kernel):
+    """Integer inputs with a scale of 1/2, 1 or 2 per channel (exact in every format): a scale
+    or bias read for the wrong channel changes the result, so this pins their indexing bit for
+    bit in every mode.  Where the intermediate of the integer case exceeds the format's exact
+    range (the dense 3x3 layer), the oracle rounds it to the storage format as the kernels do
+    (its mirror mode); the fp32 sums stay exact either way."""
+    if wl.dtype == "i8":
+        pytest.skip("INT8 scales are arbitrary fp32 values already, replicated exactly")
+    small = reduced(wl, n=2, hw=min(wl.h, 30))
+    kind = next((k for k in ("integer_pow2", "integer1_pow2") if wk.integer_safe(small, k)), None)
+    mid = "exact" if kind else small.dtype
+    case = wk.make_case(small, seed=31, kind=kind or "integer1_pow2")
+    assert len(set(np.asarray(case.s1).tolist())) == 3 and len(set(np.asarray(case.s2).tolist())) > 1
+    mod = module_or_skip(case, kernel)
+    ref = oracle_fused(case, mid=mid)
+    for mode in ("fused", "unfused"):
+        got, _ = run_case(case, mode, module=mod)
+        assert_bitexact(got, ref, small.dtype)
+    m_gpu, _ = run_case(case, "conv1", module=mod)
+    m_ref = oracle_conv1(case)
+    if mid == "exact":
+        assert_bitexact(m_gpu, m_ref, small.dtype)
+
+
+def storage_ulp(v: np.ndarray, dtype: str) -> np.ndarray:
+    """The spacing of the storage format at |v| (its subnormal spacing at 0)."""
+    mant, emin = {"f16": (10, -14), "bf16": (7, -126)}[dtype]
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** emin)))
+    return np.exp2(e - mant)
+
+
+@pytest.mark.parametrize("kernel", ["tc_roles", "tc_workers"])
+@pytest.mark.parametrize("wl", [w for w in wk.WORKLOADS if w.dtype in ("f16", "bf16")],
+                         ids=lambda w: w.name)
+def test_mirror_within_storage_ulps(cuda, wl, kernel):
+    """The tensor-core result against the oracle's mirror mode, which rounds the intermediate
+    to the storage format as the kernels do.  What remains is the kernels' fp32 sums (the
+    depthwise or dense sum, the 1x1 GEMM's accumulator) against the oracle's fp64 ones, and one
+    rounding of the output.  Bar, element by element: one storage ulp at the value, plus one
+    storage ulp at the largest output magnitude -- the room for an intermediate that rounds to
+    the other neighbour when its fp32 sum and its fp64 sum straddle a rounding boundary, which
+    moves an output near zero by many of its own ulps but by far less than the largest
+    output's ulp.  At least 99.9% of the outputs must be within one ulp of the mirror."""
+    small = reduced(wl, n=2, hw=min(wl.h, 40))
+    case = wk.make_case(small)
+    mod = module_or_skip(case, kernel)
+    got = wk.to_f64(run_case(case, "fused", module=mod)[0], small.dtype)
+    ref = oracle_fused(case, mid=small.dtype)
+    ref_s = wk.to_f64(wk.to_storage(ref, small.dtype), small.dtype)
+    err = np.abs(got - ref_s)
+    bar = storage_ulp(ref_s, small.dtype) + storage_ulp(np.abs(ref_s).max(), small.dtype)
+    worst = np.unravel_index(np.argmax(err - bar), err.shape)
+    assert np.all(err <= bar), (float(err[worst]), float(bar[worst]), float(ref[worst]))
+    within1 = float(np.mean(err <= storage_ulp(ref_s, small.dtype)))
+    assert within1 >= 0.999, within1
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
 def test_tolerance_reduced_batch(cuda, wl, kernel):
     small = reduced(wl, n=2)
     case = wk.make_case(small)
