@@ -190,9 +190,10 @@ FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, vo
  * another allocator.  `in`/`out` as for FCM_MODE_UNFUSED (caller-owned device memory).
  *  - Rejects (FCM_ERR_UNSUPPORTED) an intermediate N*Ho*Wo*Cm*element-size above 16 MiB.
  *  - The array exists once per device that loads the library and is kept until exit.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *    make that first call before any stream capture.  The current device must be the
- *    handle's device.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress),
+ *    and so does the first call after the device's context changed (cudaDeviceReset);
+ *    make those calls before any stream capture.  The current device must be the handle's
+ *    device.
  *  - Every call uses the same array and leaves its intermediate there; each call rewrites all
  *    of it before reading it.  Calls that overlap on the GPU (other streams, other handles,
  *    other threads) race on it: serialise them. */
@@ -223,7 +224,10 @@ FCM_API fcm_status fcm_plan_desc(const fcm_desc *desc, int num_sms, int smem_per
 FCM_API fcm_status fcm_tensor_bytes(const fcm_desc *desc, size_t *x_bytes, size_t *m_bytes,
                             size_t *y_bytes);
 
-/* Free the handle and everything it owns (waits for the device).  NULL is ignored. */
+/* Free the handle and everything it owns.  NULL is ignored.  The caller must first make sure
+ * that the work it enqueued with the handle has finished (synchronize the streams it passed to
+ * fcm_run / fcm_run_unfused_static): fcm_destroy waits only for the handle's own copy streams
+ * (fcm_run_host), not for the device, so that other streams of the process are not stalled. */
 FCM_API void fcm_destroy(fcm_handle *h);
 
 /* Message of the last failing call on this thread ("" if none).  Valid until the next call. */

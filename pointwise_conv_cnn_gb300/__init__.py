@@ -316,6 +316,7 @@ class FusedConvModule:
                                  addr(b2))
         self.plan = fcm_plan(self.handle)
         self.mode_bytes = mode_bytes(desc)
+        self._streams = set()   # streams work was enqueued on (waited for before destroying)
 
     def run(self, inp, out, mode: str | int = "fused", stream=None) -> None:
         """Enqueue on `stream` (torch.cuda.Stream, raw handle int, or None = current stream).
@@ -329,6 +330,7 @@ class FusedConvModule:
             s = stream.cuda_stream
         else:
             s = int(stream)
+        self._streams.add(s)
         fcm_run(self.handle, m, inp.data_ptr(), out.data_ptr(), s)
 
     def run_host(self, host_in, host_out, mode: str | int = "fused", stream=None) -> None:
@@ -347,7 +349,14 @@ class FusedConvModule:
         fcm_check(self.handle, s)
 
     def close(self) -> None:
+        """Wait for the work enqueued through run() on its streams, then free the handle
+        (fcm_destroy waits only for the handle's own copy streams)."""
         if getattr(self, "handle", None):
+            if self._streams:
+                import torch
+                for s in self._streams:
+                    torch.cuda.ExternalStream(s).synchronize()
+                self._streams.clear()
             fcm_destroy(self.handle)
             self.handle = None
 

@@ -434,7 +434,9 @@ fcm_status fcm_check(fcm_handle *h, void *stream) {
 
 void fcm_destroy(fcm_handle *h) {
     if (!h) return;
-    cudaDeviceSynchronize();
+    // the handle's own streams (fcm_run_host's copies); the caller's streams are the caller's
+    if (h->copy_in) cudaStreamSynchronize(h->copy_in);
+    if (h->copy_out) cudaStreamSynchronize(h->copy_out);
     free_handle(h);
 }
 

@@ -19,7 +19,8 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void *g_scratch_addr[kMaxDevices];   // device address of g_static_scratch, per device
+void *g_scratch_addr[kMaxDevices];             // device address of g_static_scratch, per device
+unsigned long long g_scratch_ctx[kMaxDevices];  // the context that address belongs to
 
 }  // namespace
 
@@ -42,15 +43,20 @@ extern "C" FCM_API fcm_status fcm_run_unfused_static(fcm_handle *h, const void *
         return fcm_fail(FCM_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
     void *scratch = nullptr;
     {
-        // set-up, once per device, with that device current
+        // set-up with the device current: once per device, and again whenever the device's
+        // context has changed since (a device reset loads the library's module anew, at a
+        // possibly different address); a context the driver cannot identify looks it up every
+        // time
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!g_scratch_addr[dev]) {
+        const unsigned long long ctx = fcm_current_ctx_id();
+        if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
             void *p = nullptr;
             e = cudaGetSymbolAddress(&p, g_static_scratch);
             if (e != cudaSuccess || !p)
                 return fcm_fail(FCM_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s",
                                 cudaGetErrorString(e));
             g_scratch_addr[dev] = p;
+            g_scratch_ctx[dev] = fcm_current_ctx_id();   // the runtime's context is current now
         }
         scratch = g_scratch_addr[dev];
     }
