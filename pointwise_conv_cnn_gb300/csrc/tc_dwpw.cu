@@ -89,6 +89,11 @@ Layout make_layout(const fcm_desc *d, const TcPlan &p, int cm, int mode, int sme
 
 using namespace fcm::tc;
 
+extern "C" long long fcm_model_overlap(long long, long long, long long, long long, long long,
+                                       long long, long long);
+extern "C" long long fcm_model_dwpw_gma(long long, long long, long long, long long, long long,
+                                        long long, long long, long long, long long);
+
 int fcm_tc_supported(const fcm_desc *d, int ho, int wo, int cm, const char **why) {
     auto no = [&](const char *w) {
         if (why) *why = w;
@@ -123,11 +128,22 @@ fcm_status fcm_tc_plan(const fcm_desc *d, int ho, int wo, int cm, int num_sms, i
     return fcm_tc_plan_dwpw_roles(d, ho, wo, cm, num_sms, smem_cap, p);
 }
 
+// Tile search of dwpw_kernel, after FusePlanner (section IV): every candidate tile (rows x the
+// width split evenly into tiles of at most 128 pixels) with a channel chunk that fits shared
+// memory is scored by its work efficiency (useful output pixels over the MMA rows its tiles
+// occupy); tiles within 3% of the best are admissible, and among them the planner takes the
+// smallest global-memory-access estimate of the DWPW module (the Eq. 1-4 form the plan
+// reports), then the best pipeline score (thread use of the DW warps, halo share, stages).
 fcm_status fcm_tc_plan_dwpw_roles(const fcm_desc *d, int ho, int wo, int cm, int num_sms,
                                   int smem_cap, TcPlan *p) {
     const int S = d->stride, KS = d->ksize, C = cm;
-    TcPlan best;
-    double best_score = -1.0;
+    struct Cand {
+        TcPlan t;
+        double eff, score;
+        long long gma;
+    };
+    std::vector<Cand> cands;
+    double max_eff = 0.0;
     int tw_choices[2] = {0, 0};
     int ncol_tiles = (wo + kTileM - 1) / kTileM;
     tw_choices[0] = (wo + ncol_tiles - 1) / ncol_tiles;
@@ -191,20 +207,30 @@ fcm_status fcm_tc_plan_dwpw_roles(const fcm_desc *d, int ho, int wo, int cm, int
                 }
                 t.ctas = (int)std::min<long long>(t.num_tiles, num_sms);
                 t.tmem_cols = (int)pow2_cols(2 * d->k_out);
-                // score: pixels per tile (MMA/halo efficiency) x thread efficiency x pipeline
+                // pipeline score: thread efficiency x halo share x pipeline depth x occupancy
                 double halo = (double)(th * tw * S * S) / (double)(in_rows * in_cols);
-                double score = (double)(th * tw) / kTileM * best_eff * (0.5 + 0.5 * halo) *
-                               (t.stages >= 3 ? 1.0 : 0.9) *
+                double score = best_eff * (0.5 + 0.5 * halo) * (t.stages >= 3 ? 1.0 : 0.9) *
                                (t.num_tiles >= num_sms ? 1.0 : 0.5);
-                if (score > best_score + 1e-12) {
-                    best_score = score;
-                    best = t;
-                }
+                const double eff = (double)ho * wo / ((double)t.tiles_w * t.tiles_h * kTileM);
+                const long long ov = fcm_model_overlap(d->w, d->h, (long long)tw * S,
+                                                       (long long)th * S, KS, KS, S);
+                const long long gma = fcm_model_dwpw_gma(
+                    C, ov, (long long)d->h * d->w * C, (long long)d->k_out * C,
+                    (long long)d->k_out * C, (long long)ho * wo * d->k_out, (long long)ho * wo,
+                    (long long)th * tw, (long long)C * KS * KS);
+                cands.push_back(Cand{t, eff, score, gma});
+                max_eff = std::max(max_eff, eff);
             }
         }
     }
-    if (best_score < 0) return FCM_ERR_SMEM_BUDGET;
-    *p = best;
+    const Cand *pick = nullptr;
+    for (const Cand &c : cands) {
+        if (c.eff < 0.97 * max_eff) continue;
+        if (!pick || c.gma < pick->gma || (c.gma == pick->gma && c.score > pick->score + 1e-12))
+            pick = &c;
+    }
+    if (!pick) return FCM_ERR_SMEM_BUDGET;
+    *p = pick->t;
     return FCM_OK;
 }
 

@@ -47,6 +47,28 @@ def empty(shape, dtype: str, device="cuda", fill=None):
 
 
 I8_FILL = -77
+GUARD_BYTES = 256      # guard zone on each side of an output buffer
+GUARD_BYTE = 0xA5
+
+
+def guarded_empty(shape, dtype: str, fill=None):
+    """An output tensor on the GPU inside one allocation with a guard zone of GUARD_BYTES
+    before and after it, filled with GUARD_BYTE.  Returns (tensor, check); check() raises if a
+    kernel wrote into either zone (a store outside the output it was given)."""
+    import torch
+    tdt = torch_dtype(dtype)
+    n = int(np.prod(shape)) * torch.empty((), dtype=tdt).element_size()
+    buf = torch.full((n + 2 * GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device="cuda")
+    t = buf[GUARD_BYTES:GUARD_BYTES + n].view(tdt).view(shape)
+    if fill is not None:
+        t.fill_(I8_FILL if dtype == "i8" and fill != fill else fill)
+
+    def check():
+        lo = buf[:GUARD_BYTES].cpu().numpy()
+        hi = buf[GUARD_BYTES + n:].cpu().numpy()
+        bad = int((lo != GUARD_BYTE).sum() + (hi != GUARD_BYTE).sum())
+        assert bad == 0, f"{bad} guard bytes around the output were overwritten"
+    return t, check
 
 
 def make_module(case: wk.Case, kernel: str = "auto", **desc_over) -> fcm.FusedConvModule:
@@ -63,10 +85,11 @@ def run_case(case: wk.Case, mode: str = "fused", kernel: str = "auto", inp=None,
     sh = wl.shapes()
     x = to_device(case.x if inp is None else inp, wl.dtype)
     out_shape = sh["m"] if mode == "conv1" else sh["y"]
-    y = empty(out_shape, wl.dtype, fill=float("nan"))
+    y, guards = guarded_empty(out_shape, wl.dtype, fill=float("nan"))
     mod.run(x, y, mode)
     torch.cuda.synchronize()
     mod.check()
+    guards()
     return to_host(y, wl.dtype), mod
 
 

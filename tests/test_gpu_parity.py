@@ -472,3 +472,21 @@ def test_int8_pwpw_edge_shapes(cuda, shape):
     torch.cuda.synchronize()
     mod.check()
     assert_bitexact(to_host(y, "i8"), oracle_pw(case, m_ref), "i8")
+
+
+def test_output_guards_detect_a_stray_write(cuda):
+    """The guard zones run_case puts around every output catch a write outside the output: one
+    byte just past the end (written by torch inside the same allocation) trips the check, an
+    untouched buffer passes it."""
+    import torch
+    from helpers import GUARD_BYTES, guarded_empty
+    t, check = guarded_empty((2, 3, 5, 16), "f16", fill=0.0)
+    check()
+    flat = t.view(torch.uint8).view(-1)
+    # the first byte past the output (as_strided takes an offset into the whole allocation)
+    raw = torch.as_strided(flat, (1,), (1,), flat.storage_offset() + flat.numel())
+    raw.fill_(0)
+    torch.cuda.synchronize()
+    with pytest.raises(AssertionError):
+        check()
+    assert GUARD_BYTES >= 16

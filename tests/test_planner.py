@@ -135,7 +135,7 @@ def test_int8_plans_and_refusals():
     assert pi["kernel"] == 2
     sb = 4 * (2 * i8.c + 2 * i8.k_out)
     assert pi["bytes_fused_min"] - sb == (pf["bytes_fused_min"] - sb) // 2
-    refused = [i8.with_(conv1="dense", mid=128), i8.with_(conv1="pwdw", mid=128, k_out=128),
+    refused = [i8.with_(conv1="dense", mid=128), i8.with_(conv1="pwdw", c=96, mid=128, k_out=128),
                i8.with_(c=512, k_out=64)]
     for wl in refused:
         with pytest.raises(fcm.FcmError) as e:
@@ -172,3 +172,58 @@ def test_huge_batches_plan_or_refuse_cleanly(n, ok):
         with pytest.raises(fcm.FcmError) as e:
             fcm.fcm_plan_desc(fcm.desc_from_workload(wl), 152, 232448)
         assert e.value.status == 2
+
+
+DW_DESCS = [  # (N, H, W, C, K, k, s, p, dtype)
+    (64, 56, 56, 128, 128, 3, 1, 1, "f16"),
+    (128, 112, 112, 64, 128, 3, 2, 1, "bf16"),
+    (128, 28, 28, 240, 80, 5, 1, 2, "bf16"),
+    (8, 14, 14, 256, 64, 3, 1, 1, "f16"),
+    (4, 7, 7, 96, 32, 7, 1, 3, "i8"),
+    (2, 20, 131, 64, 64, 3, 1, 1, "f16"),
+]
+
+
+def _work_eff(info, ho, wo, stencil):
+    """Useful output pixels over the MMA rows the tiles occupy (the worker-warp kernel also
+    counts the stencil pixels its 4-pixel units compute past the image)."""
+    tiles_w = -(-wo // info["tile_w"])
+    tiles_h = -(-ho // info["tile_h"])
+    eff = ho * wo / (tiles_w * tiles_h * 128)
+    if stencil:
+        pitch = info["tile_w"]   # reported as min(pitch, Wo): the pitch is a multiple of 8
+        ngroups = -(-min(pitch, wo) // 4)
+        eff *= ho * wo / (tiles_w * tiles_h * info["tile_h"] * ngroups * 4)
+    return eff
+
+
+@pytest.mark.parametrize("shape", DW_DESCS, ids=lambda s: "x".join(map(str, s[:8])) + s[8])
+@pytest.mark.parametrize("kernel", ["tc_roles", "tc_workers"])
+def test_tile_choice_minimises_the_section4_estimate(shape, kernel):
+    """The planner ranks by the bytes it models (FusePlanner, section IV): among the tiles whose
+    work efficiency is within 3% of the best one's, the chosen tile has the smallest DWPW
+    global-memory-access estimate (gma_fused_model, Eq. 1-4 form).  Every tile the kernel can
+    take is planned on its own through the tile override and compared."""
+    N, H, W, C, K, k, s, p, dt = shape
+    base = dict(n=N, h=H, w=W, c=C, k_out=K, ksize=k, stride=s, pad=p, conv1="dw", dtype=dt,
+                act1="relu", act2="none", kernel=kernel)
+    try:
+        auto = fcm.fcm_plan_desc(fcm.make_desc(**base))
+    except fcm.FcmError:
+        pytest.skip("the kernel does not take this shape")
+    ho, wo = auto["ho"], auto["wo"]
+    if kernel == "tc_workers":
+        tiles = [(32 // qw * (4 // nqx), qw * nqx) for qw in (32, 16, 8) for nqx in (1, 2, 4)]
+    else:
+        tiles = [(th, 0) for th in range(1, 129)]
+    forced = []
+    for th, tw in tiles:
+        try:
+            forced.append(fcm.fcm_plan_desc(fcm.make_desc(**dict(base, tile_h=th, tile_w=tw))))
+        except fcm.FcmError:
+            continue
+    stencil = kernel == "tc_workers"
+    best = max(_work_eff(f, ho, wo, stencil) for f in forced)
+    assert _work_eff(auto, ho, wo, stencil) >= 0.97 * best - 1e-12
+    admissible = [f for f in forced if _work_eff(f, ho, wo, stencil) >= 0.97 * best - 1e-12]
+    assert auto["gma_fused_model"] == min(f["gma_fused_model"] for f in admissible)
