@@ -105,7 +105,7 @@ def load_library(path: str | None = None):
     with _lock:
         if _lib is not None:
             return _lib
-        p = path or LIB_PATH
+        p = path or os.environ.get("FCM_LIBRARY") or LIB_PATH
         if not os.path.exists(p):
             raise FileNotFoundError(
                 f"{p} is missing: build it with `python -m pointwise_conv_cnn_gb300.build`")

@@ -1,5 +1,10 @@
 """Build libfcm.so in-tree with nvcc for sm_103a (GB300), one object per translation unit,
-compiled in parallel, then linked into a shared library next to this file."""
+compiled in parallel, then linked into a shared library next to this file.
+
+build(debug=True) builds libfcm_debug.so instead (objects in _build_debug): the same library
+with the kernels' index checks compiled in (FCM_DEBUG_CHECKS), which record the first failed
+check in the handle's error word for fcm_check to report.  Load it with load_library(path) or
+the FCM_LIBRARY environment variable."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -13,6 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfcm.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libfcm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-fvisibility=hidden",
@@ -36,16 +43,19 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every csrc/*.cu and link libfcm.so.  Returns the library path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          debug: bool = False) -> str:
+    """Compile every csrc/*.cu and link libfcm.so (libfcm_debug.so with debug=True).  Returns
+    the library path."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + (extra or [])
+    flags = NVCC_FLAGS + (extra or []) + (["-DFCM_DEBUG_CHECKS"] if debug else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -59,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

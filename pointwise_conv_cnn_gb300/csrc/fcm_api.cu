@@ -133,6 +133,7 @@ fcm_status fcm_plan(const fcm_handle *h, fcm_plan_info *info) {
 
 fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, const float *s1,
                       const float *b1, const float *s2, const float *b2, fcm_handle **out) {
+    FcmNvtxRange nvtx("fcm_create");
     if (!out) return fcm_fail(FCM_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     int ho, wo, cm;
@@ -228,8 +229,9 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
             return st;
         }
     }
-    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&h->d_err), sizeof(unsigned));
-    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(unsigned));
+    // error word: [0] flags, [1] the first failed index check of a debug build
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&h->d_err), 2 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 2 * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         free_handle(h);
@@ -290,6 +292,7 @@ static fcm_status run_one(fcm_handle *h, int mode, const void *in, void *out, cu
 }
 
 fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, void *stream) {
+    FcmNvtxRange nvtx("fcm_run");
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
     fcm_status st;
     if ((st = check_ptr(in, "in")) != FCM_OK || (st = check_ptr(out, "out")) != FCM_OK) return st;
@@ -343,6 +346,7 @@ static int host_chunks(const fcm_handle *h, int mode) {
 
 fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
                         void *stream) {
+    FcmNvtxRange nvtx("fcm_run_host");
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
     if (!host_in || !host_out) return fcm_fail(FCM_ERR_INVALID_ARG, "host buffer is NULL");
     if (mode < FCM_MODE_FUSED || mode > FCM_MODE_UNFUSED)
@@ -418,17 +422,21 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
 }
 
 fcm_status fcm_check(fcm_handle *h, void *stream) {
+    FcmNvtxRange nvtx("fcm_check");
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     FCM_CUDA(cudaStreamSynchronize(s));
-    unsigned word = 0;
-    FCM_CUDA(cudaMemcpy(&word, h->d_err, sizeof(word), cudaMemcpyDeviceToHost));
-    if (word) FCM_CUDA(cudaMemset(h->d_err, 0, sizeof(unsigned)));
+    unsigned words[2] = {0, 0};
+    FCM_CUDA(cudaMemcpy(words, h->d_err, sizeof(words), cudaMemcpyDeviceToHost));
+    const unsigned word = words[0];
+    if (word) FCM_CUDA(cudaMemset(h->d_err, 0, sizeof(words)));
     if (word & FCM_DEVERR_TIMEOUT)
         return fcm_fail(FCM_ERR_TIMEOUT, "a kernel's bounded wait ran out (error word 0x%x)", word);
     if (word)
-        return fcm_fail(FCM_ERR_DEVICE_FAULT, "a kernel's consistency check failed (error word 0x%x)",
-                        word);
+        return fcm_fail(FCM_ERR_DEVICE_FAULT,
+                        "a kernel's consistency check failed (error word 0x%x; first index check "
+                        "%u at index %u)",
+                        word, words[1] >> 24, words[1] & 0xFFFFFFu);
     return FCM_OK;
 }
 

@@ -5,7 +5,18 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fcm.h"
+
+// An NVTX range over the scope of one entry point (a profiler's timeline shows each call; with
+// no tool attached a push or pop costs one indirect call).
+struct FcmNvtxRange {
+    explicit FcmNvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~FcmNvtxRange() { nvtxRangePop(); }
+    FcmNvtxRange(const FcmNvtxRange &) = delete;
+    FcmNvtxRange &operator=(const FcmNvtxRange &) = delete;
+};
 
 // Bytes of one element of a storage type.
 inline int fcm_dtype_bytes(int dtype) { return dtype == FCM_F32 ? 4 : dtype == FCM_I8 ? 1 : 2; }

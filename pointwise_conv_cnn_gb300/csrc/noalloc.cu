@@ -26,6 +26,7 @@ unsigned long long g_scratch_ctx[kMaxDevices];  // the context that address belo
 
 extern "C" FCM_API fcm_status fcm_run_unfused_static(fcm_handle *h, const void *in, void *out,
                                                      void *stream) {
+    FcmNvtxRange nvtx("fcm_run_unfused_static");
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
     const size_t need = h->m_elems * (size_t)h->esize;
     if (need > kStaticScratchBytes)

@@ -13,6 +13,25 @@
 namespace fcm {
 namespace tc {
 
+// Index checks of a debug build (compiled with FCM_DEBUG_CHECKS; nothing in a release build).
+// A failed check never traps: it sets FCM_DEVERR_CHECK in the device error word (err[0]) and
+// records the first failure as (check id << 24) | (offending index & 0xFFFFFF) in err[1], which
+// fcm_check reports; the access itself still happens, inside the buffer the check guards.
+__device__ __forceinline__ void fcm_dcheck_fail(unsigned *err, unsigned id, unsigned idx) {
+    atomicOr(err, 2u);   // FCM_DEVERR_CHECK
+    atomicCAS(err + 1, 0u, (id << 24) | (idx & 0xFFFFFFu));
+}
+#ifdef FCM_DEBUG_CHECKS
+#define FCM_DCHECK(cond, err, id, idx)                                                 \
+    do {                                                                               \
+        if (!(cond)) fcm::tc::fcm_dcheck_fail((err), (unsigned)(id), (unsigned)(idx)); \
+    } while (0)
+#else
+#define FCM_DCHECK(cond, err, id, idx) \
+    do {                                \
+    } while (0)
+#endif
+
 // A wait gives up after this long (ns) and reports FCM_DEVERR_TIMEOUT.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 

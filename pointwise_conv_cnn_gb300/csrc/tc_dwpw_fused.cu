@@ -238,7 +238,10 @@ cudaError_t launch_tc_fused(const fcm_handle *h, const void *x, void *y, cudaStr
                               (cuuint64_t)d.n};
         cuuint64_t gstride[3] = {(cuuint64_t)d.k_out * e, (cuuint64_t)h->wo * d.k_out * e,
                                  (cuuint64_t)h->ho * h->wo * d.k_out * e};
-        cuuint32_t box[4] = {(cuuint32_t)(128 / es), (cuuint32_t)p.qw, (cuuint32_t)p.qh, 1};
+        // a quadrant of one pixel row stores only the columns inside the image (its first
+        // min(qw, Wo) staging rows); taller quadrants store their full qw x qh box, clipped
+        const int bw = p.qh == 1 ? std::min(p.qw, h->wo) : p.qw;
+        cuuint32_t box[4] = {(cuuint32_t)(128 / es), (cuuint32_t)bw, (cuuint32_t)p.qh, 1};
         cuuint32_t estr[4] = {1, 1, 1, 1};
         if (enc(&a.tmap_y, dt, 4, y, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_128B,

@@ -180,7 +180,9 @@ struct FSmem {
 template <typename T, int KS, int S, int ACT>
 __device__ __forceinline__ void fused_unit(uint32_t x_s, uint32_t row_bytes, uint32_t wdw_s,
                                            uint32_t tap_stride, const FSmem &sm, int c_glob,
-                                           uint32_t a_chunk_s, uint32_t row0, uint32_t v) {
+                                           uint32_t a_chunk_s, uint32_t row0, uint32_t v,
+                                           unsigned *a_err) {
+    (void)a_err;
     constexpr bool kI8 = std::is_same<T, int8_t>::value;
     using TM = typename std::conditional<kI8, __half, T>::type;
     constexpr uint32_t kPx = 64u * (uint32_t)sizeof(T);   // bytes of one stage pixel
@@ -235,6 +237,7 @@ __device__ __forceinline__ void fused_unit(uint32_t x_s, uint32_t row_bytes, uin
     const float4 bi1 = ldsf4(sm.b1 + 4u * (uint32_t)c_glob + 16u);
     const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
     const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
+    FCM_DCHECK(row0 + kFUnitPx <= (uint32_t)kTileM, a_err, 11, row0);   // 11: A-tile rows
 #pragma unroll
     for (int jj = 0; jj < kFUnitPx; jj++) {
         const uint32_t row = row0 + (uint32_t)jj;
@@ -512,11 +515,15 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
                         const int qd = (r >> a.lg_qh) * a.nqx + (oc0 >> a.lg_qw);
                         const uint32_t row0 = (uint32_t)((qd << 5) + ((r & ((1 << a.lg_qh) - 1)) << a.lg_qw) +
                                                          (oc0 & ((1 << a.lg_qw) - 1)));
+                        // 10: the unit's last input vector lies inside its stage
+                        FCM_DCHECK((uint32_t)((r * S + KS - 1) * a.in_cols + oc0 * S + (kFUnitPx - 1) * S + KS) *
+                                           (64u * kEs) <= a.in_stage_bytes,
+                                   a.err, 10, pg);
                         with_act(a.act1, [&](auto act_tag) {
                             constexpr int ACT1 = decltype(act_tag)::value;
                             fused_unit<T, KS, S, ACT1>(x_s, row_bytes, sm.wdw + 2u * (uint32_t)c_glob,
                                                        tap_stride, sm, c_glob, a_chunk_s, row0,
-                                                       (uint32_t)v);
+                                                       (uint32_t)v, a.err);
                         });
                     }
                     fence_proxy_async_smem();   // A visible to the tensor core
@@ -552,6 +559,7 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
                     // 16 accumulator columns from c0 -> their 16-byte chunks of the staging row
                     auto emit16 = [&](const uint32_t (&rr)[16], int c0) {
                         uint32_t pk[8];
+                        FCM_DCHECK(c0 + 16 <= a.K && (c0 >> kLgCb) < a.nblk, a.err, 12, c0);   // 12
                         fused_convert16<T, ACT2>(rr, c0, sm, pk);
                         const uint32_t blk = stage_b + (uint32_t)(c0 >> kLgCb) * 4096u;
                         const uint32_t ch = ((uint32_t)(c0 & ((1 << kLgCb) - 1)) * kEs) >> 4;

@@ -84,6 +84,10 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     const uint32_t tap_bytes = (uint32_t)a.C * 2u;   // bytes between taps of the weight image
     const uint8_t *xb = stage + g.x_off;
     const uint8_t *wb = wdw + (uint32_t)c_glob * 2u;
+    // 1: the unit's last input vector lies inside the stage
+    FCM_DCHECK(g.x_off + (uint32_t)(KS - 1) * row_bytes + (uint32_t)((kR - 1) * S + KS - 1) * px_bytes +
+                       8u * (uint32_t)sizeof(T) <= (uint32_t)a.in_stage_bytes,
+               a.err, 1, g.x_off);
 
     // INT8: the sums start at -1152 * sum(taps), the offset the widened inputs carry
     float acc[kR][8];
@@ -146,6 +150,7 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
         if (jj >= g.nvalid) break;
         const uint32_t m_row = (uint32_t)(g.m_row0 + jj);
         const int ho = ho0 + g.r, wo = wo0 + g.oc0 + jj;
+        FCM_DCHECK(m_row < (uint32_t)kTileM, a.err, 2, m_row);   // 2: A-tile row
         if constexpr (kI8) {
             float v[8];
 #pragma unroll
@@ -157,6 +162,7 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
             } else if (ho < a.Ho && wo < a.Wo) {
                 T *dst = static_cast<T *>(a.out) +
                          (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
+                FCM_DCHECK(n < a.N && c_glob + 8 <= a.C, a.err, 3, c_glob);   // 3: intermediate store
                 *reinterpret_cast<uint2 *>(dst) = make_uint2(I8::bytes4<ACT>(v[0], v[1], v[2], v[3]),
                                                              I8::bytes4<ACT>(v[4], v[5], v[6], v[7]));
             }
@@ -171,6 +177,7 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
             } else if (ho < a.Ho && wo < a.Wo) {
                 T *dst = static_cast<T *>(a.out) +
                          (((size_t)n * a.Ho + ho) * a.Wo + wo) * a.C + c_glob;
+                FCM_DCHECK(n < a.N && c_glob + 8 <= a.C, a.err, 3, c_glob);
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
