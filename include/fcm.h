@@ -168,7 +168,14 @@ FCM_API fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *
 /* Enqueue one evaluation on `stream` (a cudaStream_t; NULL = legacy default stream).
  * `in`/`out` are caller-owned device pointers as described by fcm_mode; they must not
  * overlap.  Asynchronous: returns after the launch; launch errors are reported here, errors
- * found by the kernel itself are reported by fcm_check. */
+ * found by the kernel itself are reported by fcm_check.
+ * The tensor-core kernels are launched with programmatic stream serialization allowed: one may
+ * start while the previous kernel on the stream is finishing, so that its set-up overlaps that
+ * kernel's tail, but it reads `in` and writes `out` only once that kernel has completed and its
+ * writes are visible -- stream order holds as for any launch.  Once its set-up is done it lets
+ * the next kernel on the stream start launching (griddepcontrol.launch_dependents); a kernel of
+ * the caller's that is launched with programmatic serialization allowed must therefore wait
+ * (cudaGridDependencySynchronize) before it reads `out`, as programmatic dependent launch requires of any dependent. */
 FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, void *stream);
 
 /* End-to-end variant of fcm_run on HOST buffers: copies `host_in` to a device staging buffer

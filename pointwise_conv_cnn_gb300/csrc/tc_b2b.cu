@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(std::is_same<T, int8_t>::value ? kThreadsI8 : 
     }
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t acc1_col = 0, acc2_col = 2u * (uint32_t)a.Cm;
     const unsigned long long lim = a.wait_limit_ns;
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(std::is_same<T, int8_t>::value ? kThreadsI8 : 
             if (MODE == FUSED) bulk_load(base_s + a.off_w2, a.w2_img, a.w2_bytes, bars.wbar);
             tma_prefetch_desc(&a.tmap_in);
         }
+        pdl_wait();
         int s = 0;
         uint32_t ph = 0;
         for (int lt = 0; ok && lt < my_tiles; lt++) {
@@ -708,11 +710,9 @@ namespace {
 
 template <typename T, int KS, int MODE>
 cudaError_t launch_t(const Args &a, int ctas, uint32_t smem, cudaStream_t st) {
-    auto k = b2b_kernel<T, KS, MODE>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<ctas, std::is_same<T, int8_t>::value ? kThreadsI8 : kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    static std::atomic<unsigned long long> attr_ctx{0};
+    return launch_pdl(b2b_kernel<T, KS, MODE>, attr_ctx, ctas,
+                      std::is_same<T, int8_t>::value ? kThreadsI8 : kThreads, smem, st, a);
 }
 
 template <typename T, int KS>

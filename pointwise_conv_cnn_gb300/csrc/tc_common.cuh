@@ -6,9 +6,11 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "fcm_device.cuh"
+#include "fcm_internal.h"
 
 namespace fcm {
 namespace tc {
@@ -43,6 +45,50 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
+}
+
+// ------------------------------------------------------------- programmatic dependent launch
+// The kernels are launched with programmatic stream serialization allowed (launch_pdl below):
+// a kernel may start while the previous kernel on the stream finishes, so its prologue (barrier
+// set-up, TMEM allocation, copies of the handle's weights, which no kernel writes) overlaps that
+// tail.  Before its first read of activations -- which a previous kernel may have written -- a
+// kernel waits for the previous grid to complete and its memory to be visible (pdl_wait); every
+// global write of the kernels depends on such a read.  Each CTA lets the next kernel start
+// launching once its own prologue is done (pdl_launch_dependents).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Largest dynamic shared memory of a CTA on sm_103a.
+constexpr int kSmemOptin = 227 * 1024;
+
+// Launches a persistent kernel with programmatic stream serialization allowed.  The kernel's
+// dynamic shared-memory limit is raised to kSmemOptin once per context (attr_ctx, one per kernel
+// instantiation, holds the context it was raised in): a new context -- another device, or after
+// a device reset -- raises it again.
+template <typename A>
+inline cudaError_t launch_pdl(void (*kernel)(A), std::atomic<unsigned long long> &attr_ctx,
+                              int ctas, int threads, uint32_t smem, cudaStream_t st, const A &a) {
+    if (smem > (uint32_t)kSmemOptin) return cudaErrorInvalidValue;
+    const unsigned long long ctx = fcm_current_ctx_id();
+    if (ctx == 0 || attr_ctx.load(std::memory_order_relaxed) != ctx) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin);
+        if (e != cudaSuccess) return e;
+        attr_ctx.store(ctx, std::memory_order_relaxed);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 // ------------------------------------------------------------------------------- mbarrier

@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
     }
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const unsigned long long lim = a.wait_limit_ns;
 
@@ -375,6 +376,7 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
             bulk_load(base_s + a.off_b, a.wp_img, a.wp_img_bytes, bars.wbar);
             tma_prefetch_desc(&a.tmap_x);
         }
+        pdl_wait();
         int it = 0;
         RingPos rp{0, 0u};
         TileIter ti;
@@ -613,21 +615,8 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
 
 template <typename T, int KS, int S>
 cudaError_t launch_fused(const FArgs &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
-    auto k = dwpw_fused_kernel<T, KS, S>;
-    if (smem > (uint32_t)kFSmemMax) return cudaErrorInvalidValue;
-    // The shared-memory attribute is set once per context (at the largest size any plan asks
-    // for), not on every launch; a new context (another device, or after a device reset)
-    // sets it again.
     static std::atomic<unsigned long long> attr_ctx{0};
-    const unsigned long long ctx = fcm_current_ctx_id();
-    if (ctx == 0 || attr_ctx.load(std::memory_order_relaxed) != ctx) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemMax);
-        if (e != cudaSuccess) return e;
-        attr_ctx.store(ctx, std::memory_order_relaxed);
-    }
-    k<<<ctas, threads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(dwpw_fused_kernel<T, KS, S>, attr_ctx, ctas, threads, smem, st, a);
 }
 
 #endif  // FCM_FUSED_KERNEL_BODY

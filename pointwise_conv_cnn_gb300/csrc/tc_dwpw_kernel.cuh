@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
     }
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
     const uint32_t tmem_base = has_mma ? *tmem_slot : 0u;
     const unsigned long long lim = a.wait_limit_ns;
 
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
             bulk_load(base_s + a.off_b, a.wp_img, a.wp_img_bytes, bars.wbar);
         }
         if (lane == 0) tma_prefetch_desc(&a.tmap);
+        pdl_wait();
         int it = 0;
         for (int t = blockIdx.x; ok && t < a.num_tiles; t += gridDim.x) {
             int n = 0, ho0 = 0, wo0 = 0;
@@ -589,11 +591,8 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
 // ================================================================================== host
 template <typename T, int KS, int S, int MODE, int DWB>
 cudaError_t launch_k(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
-    auto k = dwpw_kernel<T, KS, S, MODE, DWB>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<ctas, threads, smem, st>>>(a);
-    return cudaGetLastError();
+    static std::atomic<unsigned long long> attr_ctx{0};
+    return launch_pdl(dwpw_kernel<T, KS, S, MODE, DWB>, attr_ctx, ctas, threads, smem, st, a);
 }
 
 }  // namespace tc

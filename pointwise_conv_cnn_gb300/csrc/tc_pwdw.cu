@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
     }
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const unsigned long long lim = a.wait_limit_ns;
     const int my_tiles = (a.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
             bulk_load(base_s + a.off_w1, a.w1_img, a.w1_bytes, bars.wbar);
             tma_prefetch_desc(&a.tmap_x);
         }
+        pdl_wait();
         auto load8 = [&](int lt) {
             const int t = (int)blockIdx.x + lt * (int)gridDim.x;
             int n, ho0;
@@ -313,6 +315,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
             bulk_load(base_s + a.off_w1, a.w1_img, a.w1_bytes, bars.wbar);
             tma_prefetch_desc(&a.tmap_x);
         }
+        pdl_wait();
         for (int lt = 0; lt < my_tiles; lt++) {
             const int t = (int)blockIdx.x + lt * (int)gridDim.x;
             int n, ho0;
@@ -740,11 +743,8 @@ namespace {
 
 template <typename T, int KS, int S>
 cudaError_t launch_t(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
-    auto k = pwdw_kernel<T, KS, S>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<ctas, threads, smem, st>>>(a);
-    return cudaGetLastError();
+    static std::atomic<unsigned long long> attr_ctx{0};
+    return launch_pdl(pwdw_kernel<T, KS, S>, attr_ctx, ctas, threads, smem, st, a);
 }
 
 template <typename T>
