@@ -80,20 +80,23 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str, mode: str):
-    """DRAM bytes per launch from the committed ncu summary, only if it was taken on the
-    current kernel sources."""
+def ncu_traffic(workload: str, mode: str) -> dict:
+    """DRAM bytes (read + written) of one step and the bytes the step's kernels wrote (L2
+    write sectors), from the committed ncu summary, only if it was taken on the current kernel
+    sources; nulls otherwise."""
+    none = {"dram": None, "l2_write": None}
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
-        return None
+        return none
     try:
         d = json.load(open(path))
         ent = d.get(f"{workload}:{mode}")
         if ent and ent.get("source_digest") == kernel_source_digest():
-            return ent["dram_bytes_per_launch"]
-    except Exception:
+            dram = ent.get("dram_bytes_per_launch", ent.get("dram_bytes_per_step"))
+            return {"dram": dram, "l2_write": ent.get("l2_write_bytes")}
+    except (OSError, ValueError, AttributeError):
         pass
-    return None
+    return none
 
 
 class ClockSampler:
@@ -356,6 +359,7 @@ def run_ours(args):
     # the step's launches back to back inside the timed region (max over ranks): one launch of
     # the fused kernel per step in the default mode
     step_s = region_ms / steps / 1e3
+    traffic = ncu_traffic(wl.name, args.mode)
     achieved = mb["fused"] / step_s / 1e9
     e2e_ms, hb, db = time_e2e(torch, res["module"], res["case"], wl, args.mode,
                               max(5, min(100, steps // 10)), device)
@@ -379,7 +383,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 3),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": ncu_traffic(wl.name, args.mode),
+                     "traffic": traffic["dram"],
+                     "traffic_l2_write": traffic["l2_write"],
                      "bytes_per_launch": mb["fused"],
                      "step_us": round(step_s * 1e6, 3),
                      "launches_per_step": res["launches"] // steps,

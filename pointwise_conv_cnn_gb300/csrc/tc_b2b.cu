@@ -189,7 +189,7 @@ __device__ __forceinline__ void acc_to_smem_act(uint32_t taddr_row, int ncols, c
         const bool two = c0 + 16 < ncols;
         tmem_ld16(taddr_row + (uint32_t)c0, ra);
         if (two) tmem_ld16(taddr_row + (uint32_t)(c0 + 16), rb);
-        tmem_ld_wait();
+        tmem_ld_wait(ra, rb);
         emit(ra, c0);
         if (two) emit(rb, c0 + 16);
     }

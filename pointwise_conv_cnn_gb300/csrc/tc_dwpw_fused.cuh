@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kFThreads, 1) dwpw_fused_kernel(const __grid_c
                             const bool two = c0 + 16 < c_end;
                             tmem_ld16(tcol + (uint32_t)c0, ra);
                             if (two) tmem_ld16(tcol + (uint32_t)(c0 + 16), rb2);
-                            tmem_ld_wait();
+                            tmem_ld_wait(ra, rb2);
                             emit16(ra, c0);
                             if (two) emit16(rb2, c0 + 16);
                         }

@@ -19,9 +19,10 @@
 // Warp roles (persistent CTA, one per SM, static round-robin over output tiles):
 //   warp 0      TMA producer: input halo tiles (channel chunks) into a ring of stages
 //   warp 1      TMEM owner and MMA issuer (one lane issues)
-//   warps 2-5   epilogue: TMEM -> registers -> scale/bias/act -> global (warp w reads TMEM
-//               lanes 32*(w%4) .. +31)
-//   warps 6..   DW warps: stencil over a stage, result into the A tile (or HBM in DWONLY)
+//   warps 2-9   epilogue: TMEM -> registers -> scale/bias/act -> swizzled staging -> TMA
+//               stores (warp w reads TMEM lanes 32*(w%4) .. +31; the two warps of a lane
+//               quadrant convert half of the columns each)
+//   warps 10..  DW warps: stencil over a stage, result into the A tile (or HBM in DWONLY)
 // Synchronisation is by mbarriers only; every wait is bounded (about one second) and a
 // timeout sets the device error word, raises a CTA-wide abort flag and drains in-flight
 // copies and MMAs before TMEM is released.
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
                     const bool two = c0 + 16 < c_hi;
                     tmem_ld16(taddr + (uint32_t)c0, ra);
                     if (two) tmem_ld16(taddr + (uint32_t)(c0 + 16), rb);
-                    tmem_ld_wait();
+                    tmem_ld_wait(ra, rb);
                     emit16(ra, c0);
                     if (two) emit16(rb, c0 + 16);
                 }

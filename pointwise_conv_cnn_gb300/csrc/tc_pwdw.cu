@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) pwdw_kernel(const __grid_const
                             uint32_t ra[16], rb[16];
                             tmem_ld16(taddr + (uint32_t)c0, ra);
                             tmem_ld16(taddr + (uint32_t)(c0 + 16), rb);
-                            tmem_ld_wait();
+                            tmem_ld_wait(ra, rb);
                             if (pix < RQ) {
 #pragma unroll
                                 for (int h = 0; h < 2; h++) {
