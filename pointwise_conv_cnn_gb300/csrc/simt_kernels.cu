@@ -156,8 +156,10 @@ __global__ void __launch_bounds__(kThreads) k_pw(
 }
 
 // Fused conv1 -> commBuffer -> 1x1.  The commBuffer holds the intermediate of kPwPixels
-// consecutive output pixels over all Cm channels, rounded to the storage type.
-template <typename T, bool DENSE>
+// consecutive output pixels over all Cm channels, rounded to the storage type.  A depthwise
+// conv1 works on VEC channels per thread item (16-byte vectors, as k_conv1_dw does), so a tile
+// of a narrow layer is one item per thread; the per-channel arithmetic is the same either way.
+template <typename T, bool DENSE, int VEC>
 __global__ void __launch_bounds__(kThreads) k_fused(
     const T *__restrict__ x, const float *__restrict__ w1t, const float *__restrict__ s1,
     const float *__restrict__ b1, const float *__restrict__ wpt, const float *__restrict__ s2,
@@ -165,31 +167,35 @@ __global__ void __launch_bounds__(kThreads) k_fused(
     int Ho, int Wo, int k, int s, int p, int act1, int act2) {
     extern __shared__ float comm[];   // [kPwPixels][Cm]
     const long long P = (long long)N * Ho * Wo;
+    const int cv_per_px = Cm / VEC;
     for (long long blk = blockIdx.x; blk * kPwPixels < P; blk += gridDim.x) {
         long long p0 = blk * kPwPixels;
         __syncthreads();
-        for (int e = threadIdx.x; e < kPwPixels * Cm; e += blockDim.x) {
-            long long pix = p0 + e / Cm;
-            int j = e % Cm;
-            float v = 0.0f;
+        for (int e = threadIdx.x; e < kPwPixels * cv_per_px; e += blockDim.x) {
+            long long pix = p0 + e / cv_per_px;
+            const int j = (e % cv_per_px) * VEC;
+            float v[VEC];
+#pragma unroll
+            for (int q = 0; q < VEC; q++) v[q] = 0.0f;
             if (pix < P) {
                 int wo = (int)(pix % Wo);
                 long long t = pix / Wo;
                 int ho = (int)(t % Ho);
                 int n = (int)(t / Ho);
-                float acc;
+                float acc[VEC];
                 if constexpr (DENSE) {
-                    acc = dense_point<T>(x, w1t, n, ho, wo, j, H, W, C, Cm, k, s, p);
+                    acc[0] = dense_point<T>(x, w1t, n, ho, wo, j, H, W, C, Cm, k, s, p);
                 } else {
-                    float a1[1];
-                    dw_point<T, 1>(x, w1t, n, ho, wo, j, H, W, C, k, s, p, a1);
-                    acc = a1[0];
+                    dw_point<T, VEC>(x, w1t, n, ho, wo, j, H, W, C, k, s, p, acc);
                 }
                 // round to the storage type exactly as the layer-by-layer path stores it
-                v = Storage<T>::to_f(
-                    Storage<T>::from_f(act_apply(fmaf(__ldg(s1 + j), acc, __ldg(b1 + j)), act1)));
+#pragma unroll
+                for (int q = 0; q < VEC; q++)
+                    v[q] = Storage<T>::to_f(Storage<T>::from_f(
+                        act_apply(fmaf(__ldg(s1 + j + q), acc[q], __ldg(b1 + j + q)), act1)));
             }
-            comm[e] = v;
+#pragma unroll
+            for (int q = 0; q < VEC; q++) comm[(pix - p0) * Cm + j + q] = v[q];
         }
         __syncthreads();
         pw_tile<T>(comm, p0, P, Cm, K, wpt, s2, b2, act2, y);
@@ -292,25 +298,20 @@ cudaError_t fused_t(const fcm_handle *h, const void *xin, void *yout, cudaStream
     size_t smem = sizeof(float) * kPwPixels * h->cm;
     long long blocks = (P + kPwPixels - 1) / kPwPixels;
     int grid = (int)(blocks < (long long)h->num_sms * 8 ? blocks : (long long)h->num_sms * 8);
-    cudaError_t e;
-    if (d.conv1 == FCM_CONV1_DENSE) {
-        e = cudaFuncSetAttribute(k_fused<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+    auto launch = [&](auto kernel) -> cudaError_t {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        k_fused<T, true><<<grid, kThreads, smem, st>>>(
+        kernel<<<grid, kThreads, smem, st>>>(
             static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
             static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, d.k_out, h->ho, h->wo, d.ksize,
             d.stride, d.pad, d.act1, d.act2);
-    } else {
-        e = cudaFuncSetAttribute(k_fused<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        k_fused<T, false><<<grid, kThreads, smem, st>>>(
-            static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
-            static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, d.k_out, h->ho, h->wo, d.ksize,
-            d.stride, d.pad, d.act1, d.act2);
-    }
-    return cudaGetLastError();
+        return cudaGetLastError();
+    };
+    constexpr int V16 = 16 / (int)sizeof(T);
+    if (d.conv1 == FCM_CONV1_DENSE) return launch(k_fused<T, true, 1>);
+    if (h->cm % V16 == 0) return launch(k_fused<T, false, V16>);
+    return launch(k_fused<T, false, 1>);
 }
 
 // PWDW layer by layer: the 1x1 convolution x -> m [N,H,W,Cm] (k_pw with C inputs), then the
