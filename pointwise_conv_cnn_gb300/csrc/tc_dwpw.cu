@@ -365,6 +365,8 @@ namespace {
 template <typename T, int KS, int S, int MODE>
 cudaError_t launch_t(const Args &a, int ctas, int threads, uint32_t smem, cudaStream_t st) {
     if constexpr (KS <= 3 && MODE != PWONLY) {
+        if (a.dw_per_chunk > 0 && KS == 3 && MODE != PWONLY && threads <= kMaxThreadsBound2)
+            return launch_k<T, KS, S, MODE, 2>(a, ctas, threads, smem, st);
         if (a.dw_per_chunk > 0) return launch_k<T, KS, S, MODE, 1>(a, ctas, threads, smem, st);
     }
     return launch_k<T, KS, S, MODE, 0>(a, ctas, threads, smem, st);

@@ -25,6 +25,11 @@ constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);
 // up to 14 DW warps, 20 in all, 96 registers a thread.
 constexpr int kMaxDwWarpsBound = 14;
 constexpr int kMaxThreadsBound = 32 * (kFirstDwWarp + kMaxDwWarpsBound);
+// Chunk-bound plans of a single 64-channel chunk (7 stencil warps for a 112-pixel tile) launch
+// at most this many threads; their instantiations (DWB = 2) are compiled for it, so a thread
+// gets 120 registers instead of the 80 that 768 threads leave.
+constexpr int kMaxDwWarpsBound2 = 7;
+constexpr int kMaxThreadsBound2 = 32 * (kFirstDwWarp + kMaxDwWarpsBound2);
 constexpr int kR = 4;          // output pixels per DW work unit (along W)
 constexpr int kTileM = 128;    // MMA M: pixels per output tile (padded)
 constexpr int kMaxStages = 8;

@@ -26,6 +26,11 @@ FCM_INST(__nv_bfloat16, 3, 2, DWONLY, 0)
 FCM_INST(__nv_bfloat16, 3, 2, DWONLY, 1)
 FCM_INST(__nv_bfloat16, 1, 1, PWONLY, 0)
 
+FCM_INST(__nv_bfloat16, 3, 1, FUSED, 2)
+FCM_INST(__nv_bfloat16, 3, 1, DWONLY, 2)
+FCM_INST(__nv_bfloat16, 3, 2, FUSED, 2)
+FCM_INST(__nv_bfloat16, 3, 2, DWONLY, 2)
+
 #undef FCM_INST
 
 }  // namespace tc

@@ -25,6 +25,11 @@ FCM_INST(int8_t, 3, 2, FUSED, 1)
 FCM_INST(int8_t, 3, 2, DWONLY, 0)
 FCM_INST(int8_t, 3, 2, DWONLY, 1)
 
+FCM_INST(int8_t, 3, 1, FUSED, 2)
+FCM_INST(int8_t, 3, 1, DWONLY, 2)
+FCM_INST(int8_t, 3, 2, FUSED, 2)
+FCM_INST(int8_t, 3, 2, DWONLY, 2)
+
 #undef FCM_INST
 
 }  // namespace tc

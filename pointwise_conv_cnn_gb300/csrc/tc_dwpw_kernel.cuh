@@ -192,9 +192,10 @@ __device__ __forceinline__ void tile_coords(const Args &a, int t, int &n, int &h
     wo0 = (rem % a.tiles_w) * a.tile_w;
 }
 
-// DWB: chunk-bound DW warps (Args::dw_per_chunk > 0), with their own register budget.
+// DWB: chunk-bound DW warps (Args::dw_per_chunk > 0), with their own register budget: 1 for
+// up to kMaxThreadsBound threads, 2 for up to kMaxThreadsBound2.
 template <typename T, int KS, int S, int MODE, int DWB>
-__global__ void __launch_bounds__(DWB ? kMaxThreadsBound : kMaxThreads, 1)
+__global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThreadsBound : kMaxThreads, 1)
     dwpw_kernel(const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
