@@ -15,6 +15,8 @@
 // so fused == conv1-then-PW bit for bit.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "fcm_device.cuh"
 #include "fcm_internal.h"
 
@@ -241,6 +243,72 @@ __global__ void __launch_bounds__(kThreads) k_fused_pwdw(
     }
 }
 
+// PWDW in one pass with the intermediate tiled in shared memory: a block takes TH output rows
+// of one image over the full width and CC intermediate channels.  It first computes the
+// intermediate over the rows and columns those outputs read (the 1x1 convolution of each input
+// pixel there, rounded to the storage type, as the layer-by-layer path stores it; zero where the
+// depthwise layer pads), then the depthwise layer from shared memory.  Each intermediate value
+// is computed once per block instead of once per depthwise tap, and the per-element arithmetic
+// is that of k_pw followed by k_conv1_dw, so fused == unfused bit for bit.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_fused_pwdw_tiled(
+    const T *__restrict__ x, const float *__restrict__ wq, const float *__restrict__ s1,
+    const float *__restrict__ b1, const float *__restrict__ wd, const float *__restrict__ s2,
+    const float *__restrict__ b2, T *__restrict__ y, int N, int H, int W, int C, int Cm, int Ho,
+    int Wo, int k, int s, int p, int act1, int act2, int TH, int CC) {
+    extern __shared__ float mt[];   // [R][Q][CC]: halo rows x halo columns x channels
+    const int R = (TH - 1) * s + k, Q = (Wo - 1) * s + k;
+    const int row_tiles = (Ho + TH - 1) / TH, ch_tiles = (Cm + CC - 1) / CC;
+    const long long blocks = (long long)N * row_tiles * ch_tiles;
+    for (long long b = blockIdx.x; b < blocks; b += gridDim.x) {
+        const int ct = (int)(b % ch_tiles);
+        const long long rest = b / ch_tiles;
+        const int rt = (int)(rest % row_tiles);
+        const int n = (int)(rest / row_tiles);
+        const int ho0 = rt * TH, j0 = ct * CC;
+        const int hi0 = ho0 * s - p, wi0 = -p;
+        __syncthreads();
+        for (int e = threadIdx.x; e < R * Q * CC; e += blockDim.x) {
+            const int jj = e % CC;
+            const int q = (e / CC) % Q;
+            const int r = e / (CC * Q);
+            const int hi = hi0 + r, wi = wi0 + q, j = j0 + jj;
+            float v = 0.0f;
+            if (hi >= 0 && hi < H && wi >= 0 && wi < W && j < Cm) {
+                const T *xp = x + (((size_t)n * H + hi) * W + wi) * C;
+                float acc = 0.0f;
+                for (int c = 0; c < C; c++)
+                    acc = fmaf(Storage<T>::to_f(xp[c]), __ldg(wq + (size_t)c * Cm + j), acc);
+                v = Storage<T>::to_f(Storage<T>::from_f(
+                    act_apply(fmaf(__ldg(s1 + j), acc, __ldg(b1 + j)), act1)));
+            }
+            mt[e] = v;
+        }
+        __syncthreads();
+        const int rows = min(TH, Ho - ho0);
+        for (int e = threadIdx.x; e < rows * Wo * CC; e += blockDim.x) {
+            const int jj = e % CC;
+            const int wo = (e / CC) % Wo;
+            const int r = e / (CC * Wo);
+            const int j = j0 + jj, ho = ho0 + r;
+            if (j >= Cm) continue;
+            float acc = 0.0f;
+            for (int i = 0; i < k; i++) {
+                const int hi = ho * s - p + i;
+                if (hi < 0 || hi >= H) continue;
+                for (int u = 0; u < k; u++) {
+                    const int wi = wo * s - p + u;
+                    if (wi < 0 || wi >= W) continue;
+                    const float mv = mt[((r * s + i) * Q + wo * s + u) * CC + jj];
+                    acc = fmaf(mv, __ldg(wd + (size_t)(i * k + u) * Cm + j), acc);
+                }
+            }
+            y[(((size_t)n * Ho + ho) * Wo + wo) * Cm + j] =
+                Storage<T>::from_f(act_apply(fmaf(__ldg(s2 + j), acc, __ldg(b2 + j)), act2));
+        }
+    }
+}
+
 int grid_for(long long work_items, int threads, int num_sms) {
     long long blocks = (work_items + threads - 1) / threads;
     long long cap = (long long)num_sms * 8;
@@ -354,6 +422,26 @@ cudaError_t pwdw_second_t(const fcm_handle *h, const void *min, void *yout, cuda
 template <typename T>
 cudaError_t pwdw_fused_t(const fcm_handle *h, const void *xin, void *yout, cudaStream_t st) {
     const fcm_desc &d = h->d;
+    // the tiled kernel with the largest channel slice whose intermediate tile fits 96 KB of
+    // shared memory (four output rows a block, fewer for short images)
+    const int TH = std::min(4, h->ho);
+    const long long R = (long long)(TH - 1) * d.stride + d.ksize;
+    const long long Q = (long long)(h->wo - 1) * d.stride + d.ksize;
+    for (int CC = 32; CC >= 1; CC >>= 1) {
+        const long long smem = R * Q * CC * (long long)sizeof(float);
+        if (smem > 96 * 1024) continue;
+        cudaError_t e = cudaFuncSetAttribute(k_fused_pwdw_tiled<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const long long blocks = (long long)d.n * ((h->ho + TH - 1) / TH) * ((h->cm + CC - 1) / CC);
+        const int grid = (int)std::min<long long>(blocks, (long long)h->num_sms * 8);
+        k_fused_pwdw_tiled<T><<<grid, kThreads, (size_t)smem, st>>>(
+            static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
+            static_cast<T *>(yout), d.n, d.h, d.w, d.c, h->cm, h->ho, h->wo, d.ksize, d.stride,
+            d.pad, d.act1, d.act2, TH, CC);
+        return cudaGetLastError();
+    }
+    // a row of the halo does not fit even one channel: one thread per output element
     long long items = (long long)d.n * h->ho * h->wo * h->cm;
     k_fused_pwdw<T><<<grid_for(items, kThreads, h->num_sms), kThreads, 0, st>>>(
         static_cast<const T *>(xin), h->w1t, h->s1, h->b1, h->wpt, h->s2, h->b2,
