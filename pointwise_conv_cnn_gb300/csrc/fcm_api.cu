@@ -222,6 +222,10 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
         free_handle(h);
         return st;
     }
+    if (K <= 128) {
+        memcpy(h->b2_host, hb2.data(), sizeof(float) * (size_t)K);
+        h->b2_host_of = h->b2;
+    }
     if (h->plan.kernel == FCM_KERNEL_TC) {
         st = fcm_tc_prepare(h, hw1.data(), hwp.data());
         if (st != FCM_OK) {

@@ -81,6 +81,10 @@ struct fcm_handle {
     void *w1dw_pad = nullptr; // the same taps as [k*k][Cp], Cp = C rounded up to 64, zero-padded
                               // (dwpw_fused_kernel); INT8 PW-only views point it at i8_idtap
     float *s1 = nullptr, *b1 = nullptr, *s2 = nullptr, *b2 = nullptr;
+    // host copy of the second layer's biases (K <= 128), valid for the device array b2_host_of
+    // points to; the DW->PW role kernel passes them as kernel parameters
+    float b2_host[128] = {};
+    const float *b2_host_of = nullptr;
     // INT8: 1152 * (sum of each channel's taps), and the identity stencil (one f16 tap of 1,
     // scale 1, bias 0, offset 1152) through which the PW-only mode runs on the fused kernel
     float *q1 = nullptr;

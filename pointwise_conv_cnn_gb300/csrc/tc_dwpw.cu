@@ -455,6 +455,11 @@ cudaError_t launch_mode(const fcm_handle *h, int mode, const void *in, void *out
     a.b1 = h->b1;
     a.s2 = h->s2;
     a.b2 = h->b2;
+    if (h->b2 && h->b2 == h->b2_host_of && (d.k_out == 64 || d.k_out == 128) &&
+        d.k_out <= kMaxBiasParams) {
+        memcpy(a.b2c, h->b2_host, sizeof(float) * (size_t)d.k_out);
+        a.b2c_n = d.k_out;
+    }
     a.q1 = h->q1;
     a.err = h->d_err;
     a.wait_limit_ns = kWaitLimitNs;

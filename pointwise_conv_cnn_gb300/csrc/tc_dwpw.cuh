@@ -37,6 +37,8 @@ constexpr int kMaxChunks = 16;
 
 enum Mode { FUSED = 0, DWONLY = 1, PWONLY = 2 };
 
+constexpr int kMaxBiasParams = 128;   // biases passed as kernel parameters (Args::b2c)
+
 struct Args {
     CUtensorMap tmap;          // x (FUSED/DWONLY: 4-D C,W,H,N) or m (PWONLY: 2-D C,P)
     CUtensorMap tmap_out;      // y: 4-D K,Wo,Ho,N box (64,tile_w,tile_h,1) or 2-D K,P box (64,128)
@@ -59,6 +61,11 @@ struct Args {
     uint32_t off_b, off_a, off_in, in_stage_stride, off_out, off_wdw, off_sb, off_bar;
     int out_bufs;              // output staging tiles (2: a tile's stores overlap the next tile)
     uint32_t out_buf_bytes;
+    // The 1x1's biases as kernel parameters (b2c_n = K when K is 64 or 128, else 0): the
+    // epilogue's FMAs then read them as constant operands instead of loading them from shared
+    // memory (measured on the MobileNet layer: 30.6 us against 32.0 us a launch)
+    int b2c_n;
+    float b2c[kMaxBiasParams];
 };
 
 struct Bars {

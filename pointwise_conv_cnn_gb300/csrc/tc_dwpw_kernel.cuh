@@ -459,6 +459,68 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                     tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)ab * (a.tmem_cols >> 1);
                 // two loads of 16 columns, one wait (K is a multiple of 16; keeping a load in
                 // flight across the conversion measured slower)
+                // The same on compile-time columns, with the biases from the kernel parameters
+                // (used when K is 64 or 128: each warp's column range is then fixed at compile
+                // time up to the choice of its half).
+                auto emit16c = [&](const uint32_t (&rr)[16], auto c0t) {
+                    constexpr int C0 = decltype(c0t)::value;
+                    if constexpr (kI8) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; i4++) {
+                            const float4 sc = *reinterpret_cast<const float4 *>(s2_s + C0 + 4 * i4);
+                            pk[i4] = I8::bytes4<ACT>(
+                                fmaf(sc.x, __uint_as_float(rr[4 * i4]), a.b2c[C0 + 4 * i4]),
+                                fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), a.b2c[C0 + 4 * i4 + 1]),
+                                fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), a.b2c[C0 + 4 * i4 + 2]),
+                                fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), a.b2c[C0 + 4 * i4 + 3]));
+                        }
+                        constexpr uint32_t blk = (uint32_t)(C0 >> 6) * kBlockBytes;
+                        constexpr uint32_t ch = (uint32_t)((C0 & 63) >> 4);
+                        sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+                    } else {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; i4++) {
+                            const float4 sc = *reinterpret_cast<const float4 *>(s2_s + C0 + 4 * i4);
+                            const float y0 = fmaf(sc.x, __uint_as_float(rr[4 * i4]), a.b2c[C0 + 4 * i4]);
+                            const float y1 = fmaf(sc.y, __uint_as_float(rr[4 * i4 + 1]), a.b2c[C0 + 4 * i4 + 1]);
+                            const float y2 = fmaf(sc.z, __uint_as_float(rr[4 * i4 + 2]), a.b2c[C0 + 4 * i4 + 2]);
+                            const float y3 = fmaf(sc.w, __uint_as_float(rr[4 * i4 + 3]), a.b2c[C0 + 4 * i4 + 3]);
+                            pk[2 * i4] = Pack2<TS>::template run<ACT>(y0, y1);
+                            pk[2 * i4 + 1] = Pack2<TS>::template run<ACT>(y2, y3);
+                        }
+                        constexpr uint32_t blk = (uint32_t)(C0 >> 6) * kBlockBytes;
+                        constexpr uint32_t ch = (uint32_t)((C0 & 63) >> 3);
+                        sts128(row_s + blk + ((ch ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+                        sts128(row_s + blk + (((ch + 1) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
+                    }
+                };
+                // 32 columns from compile-time column C0: two 16-column loads, one wait
+                auto cols32 = [&](auto c0t) {
+                    constexpr int C0 = decltype(c0t)::value;
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16(taddr + (uint32_t)C0, ra);
+                    tmem_ld16(taddr + (uint32_t)(C0 + 16), rb);
+                    tmem_ld_wait(ra, rb);
+                    emit16c(ra, std::integral_constant<int, C0>{});
+                    emit16c(rb, std::integral_constant<int, C0 + 16>{});
+                };
+                static_assert(kEpiWarps == 8, "two epilogue warps per lane quadrant");
+                if (a.b2c_n == 128 && a.K == 128) {
+                    if (part == 0) {
+                        cols32(std::integral_constant<int, 0>{});
+                        cols32(std::integral_constant<int, 32>{});
+                    } else {
+                        cols32(std::integral_constant<int, 64>{});
+                        cols32(std::integral_constant<int, 96>{});
+                    }
+                } else if (a.b2c_n == 64 && a.K == 64) {
+                    if (part == 0)
+                        cols32(std::integral_constant<int, 0>{});
+                    else
+                        cols32(std::integral_constant<int, 32>{});
+                } else
                 for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                     uint32_t ra[16], rb[16];
                     const bool two = c0 + 16 < c_hi;
