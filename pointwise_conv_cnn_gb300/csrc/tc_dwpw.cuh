@@ -18,6 +18,10 @@ namespace tc {
 // so the chunk-bound DW warps read their taps from shared memory instead of holding them.
 constexpr int kEpiWarps = 8;
 constexpr bool kDwTapsInRegs = false;
+// Chunk-bound DW warps (768-thread tier, 16-bit storage) hold their channels' scale and bias
+// in registers instead of loading them for every unit (MobileNet layer: 29.8 us against 30.8 us
+// a launch, back to back).
+constexpr bool kDwNormInRegs = true;
 constexpr int kFirstDwWarp = 2 + kEpiWarps;
 constexpr int kMaxDwWarps = 10;   // 16 warps in all: up to 128 registers a thread
 constexpr int kMaxThreads = 32 * (kFirstDwWarp + kMaxDwWarps);

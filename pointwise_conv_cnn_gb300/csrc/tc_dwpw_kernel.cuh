@@ -71,12 +71,18 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
 // C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
 // which clobber memory).  INT8: 8-byte input vectors widened to f16 (1152 + x), f16 taps, and
 // the sums started at -1152 * sum(taps) of each channel (q1_s), which the offsets cancel.
-template <typename T, int KS, int S, int MODE, int ACT, bool RT>
+// The first layer's scale, bias and (INT8) sum offset of a unit's 8 channels, held in
+// registers by a chunk-bound stencil thread, whose channels never change.
+struct DwNorm {
+    float s[8], b[8], q[8];
+};
+
+template <typename T, int KS, int S, int MODE, int ACT, bool RT, bool NR>
 __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chunk,
                                         const uint8_t *stage, const uint8_t *wdw,
-                                        const uint4 (&wreg)[KS * KS], const float *s1_s,
-                                        const float *b1_s, const float *q1_s, uint32_t a_saddr,
-                                        int n, int ho0, int wo0) {
+                                        const uint4 (&wreg)[KS * KS], const DwNorm &nr,
+                                        const float *s1_s, const float *b1_s, const float *q1_s,
+                                        uint32_t a_saddr, int n, int ho0, int wo0) {
     constexpr bool kI8 = std::is_same<T, int8_t>::value;
     using TM = typename std::conditional<kI8, __half, T>::type;   // arithmetic type
     const int c_glob = chunk * a.chunk_c + g.cv;
@@ -93,9 +99,17 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     // INT8: the sums start at -1152 * sum(taps), the offset the widened inputs carry
     float acc[kR][8];
     if constexpr (kI8) {
-        const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
-        const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
-        const float qq[8] = {-q0.x, -q0.y, -q0.z, -q0.w, -q1.x, -q1.y, -q1.z, -q1.w};
+        float qq[8];
+        if constexpr (NR) {
+#pragma unroll
+            for (int c = 0; c < 8; c++) qq[c] = -nr.q[c];
+        } else {
+            const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
+            const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
+            const float qv[8] = {-q0.x, -q0.y, -q0.z, -q0.w, -q1.x, -q1.y, -q1.z, -q1.w};
+#pragma unroll
+            for (int c = 0; c < 8; c++) qq[c] = qv[c];
+        }
 #pragma unroll
         for (int jj = 0; jj < kR; jj++)
 #pragma unroll
@@ -137,12 +151,26 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
             }
         }
     }
-    const float4 sc0 = *reinterpret_cast<const float4 *>(s1_s + c_glob);
-    const float4 sc1 = *reinterpret_cast<const float4 *>(s1_s + c_glob + 4);
-    const float4 bi0 = *reinterpret_cast<const float4 *>(b1_s + c_glob);
-    const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
-    const float sc[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
-    const float bi[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
+    float sc[8], bi[8];
+    if constexpr (NR) {
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            sc[c] = nr.s[c];
+            bi[c] = nr.b[c];
+        }
+    } else {
+        const float4 sc0 = *reinterpret_cast<const float4 *>(s1_s + c_glob);
+        const float4 sc1 = *reinterpret_cast<const float4 *>(s1_s + c_glob + 4);
+        const float4 bi0 = *reinterpret_cast<const float4 *>(b1_s + c_glob);
+        const float4 bi1 = *reinterpret_cast<const float4 *>(b1_s + c_glob + 4);
+        const float sv[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
+        const float bv[8] = {bi0.x, bi0.y, bi0.z, bi0.w, bi1.x, bi1.y, bi1.z, bi1.w};
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+            sc[c] = sv[c];
+            bi[c] = bv[c];
+        }
+    }
     // A-tile address of (row, c_glob): 64-channel block, 128-byte row, swizzled 16-byte chunk
     const uint32_t a_blk = a_saddr + (uint32_t)(c_glob >> 6) * (kTileM * 128u);
     const uint32_t a_chunk = (uint32_t)(c_glob >> 3) & 7u;
@@ -573,6 +601,19 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                 for (int t = 0; t < KS * KS; t++)
                     wreg[t] = *reinterpret_cast<const uint4 *>(wb + (uint32_t)t * (uint32_t)a.C * 2u);
             }
+            // (not for INT8, whose offsets would add eight more registers, nor for the 544-thread
+            // tier, which then spills: both measured slower)
+            constexpr bool kNormRegs = kDwNormInRegs && !kI8 && DWB == 1;
+            DwNorm nreg;
+            if (kNormRegs) {
+                const int cg = jm * a.chunk_c + g0.cv;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    nreg.s[c] = s1_s[cg + c];
+                    nreg.b[c] = b1_s[cg + c];
+                    nreg.q[c] = kI8 ? q1_s[cg + c] : 0.0f;
+                }
+            }
             with_act(a.act1, [&](auto act_tag) {
                 constexpr int ACT = decltype(act_tag)::value;
                 int lt = 0;
@@ -588,7 +629,7 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                         break;
                     const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
                     if (has_unit)
-                        dw_unit<T, KS, S, MODE, ACT, kDwTapsInRegs>(a, g0, jm, stage_g, wdw_g, wreg, s1_s,
+                        dw_unit<T, KS, S, MODE, ACT, kDwTapsInRegs, kNormRegs>(a, g0, jm, stage_g, wdw_g, wreg, nreg, s1_s,
                                                            b1_s, q1_s, a_s, n, ho0, wo0);
                     if (MODE == FUSED) fence_proxy_async_smem();
                     __syncwarp();
@@ -603,6 +644,7 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
             const int tid = (warp - kFirstDwWarp) * 32 + lane;
             const int nthr = a.n_dw_warps * 32;
             const uint4 wnone[KS * KS] = {};
+            const DwNorm nnone{};
             // the thread's first unit (most plans give each thread at most one per chunk)
             const DwUnit g0 = dw_unit_geom<T, S>(a, tid < units ? tid : 0);
             with_act(a.act1, [&](auto act_tag) {
@@ -626,11 +668,11 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                         }
                         const uint8_t *stage_g = base_g + a.off_in + (uint32_t)s * a.in_stage_stride;
                         if (tid < units)
-                            dw_unit<T, KS, S, MODE, ACT, false>(a, g0, j, stage_g, wdw_g, wnone, s1_s,
+                            dw_unit<T, KS, S, MODE, ACT, false, false>(a, g0, j, stage_g, wdw_g, wnone, nnone, s1_s,
                                                                 b1_s, q1_s, a_s, n, ho0, wo0);
                         for (int u = tid + nthr; u < units; u += nthr)
-                            dw_unit<T, KS, S, MODE, ACT, false>(a, dw_unit_geom<T, S>(a, u), j, stage_g,
-                                                                wdw_g, wnone, s1_s, b1_s, q1_s, a_s,
+                            dw_unit<T, KS, S, MODE, ACT, false, false>(a, dw_unit_geom<T, S>(a, u), j, stage_g,
+                                                                wdw_g, wnone, nnone, s1_s, b1_s, q1_s, a_s,
                                                                 n, ho0, wo0);
                         if (MODE == FUSED) fence_proxy_async_smem();
                         __syncwarp();
