@@ -71,10 +71,10 @@ __device__ __forceinline__ DwUnit dw_unit_geom(const Args &a, int u) {
 // C++ loads so that the compiler may schedule them early (they stay after the mbarrier waits,
 // which clobber memory).  INT8: 8-byte input vectors widened to f16 (1152 + x), f16 taps, and
 // the sums started at -1152 * sum(taps) of each channel (q1_s), which the offsets cancel.
-// The first layer's scale, bias and (INT8) sum offset of a unit's 8 channels, held in
-// registers by a chunk-bound stencil thread, whose channels never change.
+// The first layer's scale and bias of a unit's 8 channels, held in registers by a chunk-bound
+// stencil thread, whose channels never change.
 struct DwNorm {
-    float s[8], b[8], q[8];
+    float s[8], b[8];
 };
 
 template <typename T, int KS, int S, int MODE, int ACT, bool RT, bool NR>
@@ -100,10 +100,7 @@ __device__ __forceinline__ void dw_unit(const Args &a, const DwUnit &g, int chun
     float acc[kR][8];
     if constexpr (kI8) {
         float qq[8];
-        if constexpr (NR) {
-#pragma unroll
-            for (int c = 0; c < 8; c++) qq[c] = -nr.q[c];
-        } else {
+        {
             const float4 q0 = *reinterpret_cast<const float4 *>(q1_s + c_glob);
             const float4 q1 = *reinterpret_cast<const float4 *>(q1_s + c_glob + 4);
             const float qv[8] = {-q0.x, -q0.y, -q0.z, -q0.w, -q1.x, -q1.y, -q1.z, -q1.w};
@@ -601,9 +598,9 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                 for (int t = 0; t < KS * KS; t++)
                     wreg[t] = *reinterpret_cast<const uint4 *>(wb + (uint32_t)t * (uint32_t)a.C * 2u);
             }
-            // (not for INT8, whose offsets would add eight more registers, nor for the 544-thread
-            // tier, which then spills: both measured slower)
-            constexpr bool kNormRegs = kDwNormInRegs && !kI8 && DWB == 1;
+            // (16-bit storage in the fused mode of the 768-thread tier: INT8, the 544-thread tier
+            // and the depthwise-only mode spill far more with them and measured slower)
+            constexpr bool kNormRegs = kDwNormInRegs && !kI8 && DWB == 1 && MODE == FUSED;
             DwNorm nreg;
             if (kNormRegs) {
                 const int cg = jm * a.chunk_c + g0.cv;
@@ -611,7 +608,6 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                 for (int c = 0; c < 8; c++) {
                     nreg.s[c] = s1_s[cg + c];
                     nreg.b[c] = b1_s[cg + c];
-                    nreg.q[c] = kI8 ? q1_s[cg + c] : 0.0f;
                 }
             }
             with_act(a.act1, [&](auto act_tag) {
