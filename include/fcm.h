@@ -188,6 +188,19 @@ FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, v
 FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
                         void *stream);
 
+/* fcm_run_host without the wait: enqueues the same copies and kernels and returns.  The result
+ * is in `host_out` once `stream` has completed the work enqueued so far (cudaStreamSynchronize,
+ * or an event recorded on `stream` after the call).  Until then `host_in` must not change and
+ * `host_out` must not be read.  The input copies are ordered after this handle's previous host
+ * calls (chunk by chunk when the batch is split the same way, so that one call's output copies
+ * overlap the next call's input copies, and after all of the previous call's output copies when
+ * `host_in` overlaps its `host_out`), but not after other work on `stream`: the caller orders
+ * the producers of `host_in` itself.  Consecutive calls on one handle may therefore be in
+ * flight together; they must come from one host thread.  Pinned host memory is required for
+ * the copies to overlap. */
+FCM_API fcm_status fcm_run_host_async(fcm_handle *h, int mode, const void *host_in,
+                                      void *host_out, void *stream);
+
 /* Layer-by-layer evaluation that allocates nothing: the same result as fcm_run with
  * FCM_MODE_UNFUSED, but the intermediate is kept in a fixed 16 MiB device array compiled into
  * the library instead of a buffer the handle allocates on first use.  The paper has no

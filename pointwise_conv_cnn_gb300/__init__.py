@@ -16,7 +16,8 @@ import threading
 
 __all__ = [
     "FCM_OK", "FcmError", "FcmDesc", "FcmPlanInfo", "FusedConvModule", "load_library",
-    "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
+    "fcm_create", "fcm_run", "fcm_run_host", "fcm_run_host_async", "fcm_check", "fcm_plan",
+    "fcm_plan_desc",
     "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_model_pwdw_gma",
     "fcm_model_pwpw_gma", "fcm_fuse_plan", "FcmLayer", "FcmLayerPlan", "LAYER_KINDS", "MODULES",
@@ -40,8 +41,8 @@ MODES = {"fused": 0, "conv1": 1, "pw": 2, "unfused": 3}
 KERNELS = {"auto": 0, "simt": 1, "tc": 2, "tc_roles": 3, "tc_workers": 4}
 
 EXPORTED_SYMBOLS = (
-    "fcm_create", "fcm_run", "fcm_run_host", "fcm_check", "fcm_plan", "fcm_plan_desc",
-    "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
+    "fcm_create", "fcm_run", "fcm_run_host", "fcm_run_host_async", "fcm_check", "fcm_plan",
+    "fcm_plan_desc", "fcm_tensor_bytes", "fcm_destroy", "fcm_last_error", "fcm_model_overlap",
     "fcm_model_pw_gma", "fcm_model_dw_gma", "fcm_model_dwpw_gma", "fcm_run_unfused_static",
     "fcm_selftest_wait_timeout",
     "fcm_model_pwdw_gma", "fcm_model_pwpw_gma", "fcm_fuse_plan",
@@ -116,13 +117,15 @@ def load_library(path: str | None = None):
                                    ctypes.POINTER(vp)]
         lib.fcm_run.argtypes = [vp, i, vp, vp, vp]
         lib.fcm_run_host.argtypes = [vp, i, vp, vp, vp]
+        lib.fcm_run_host_async.argtypes = [vp, i, vp, vp, vp]
         lib.fcm_run_unfused_static.argtypes = [vp, vp, vp, vp]
         lib.fcm_check.argtypes = [vp, vp]
         lib.fcm_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong]
         lib.fcm_plan.argtypes = [vp, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_plan_desc.argtypes = [ctypes.POINTER(FcmDesc), i, i, ctypes.POINTER(FcmPlanInfo)]
         lib.fcm_tensor_bytes.argtypes = [ctypes.POINTER(FcmDesc)] + [ctypes.POINTER(ctypes.c_size_t)] * 3
-        for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_run_unfused_static", "fcm_check", "fcm_plan",
+        for f in ("fcm_create", "fcm_run", "fcm_run_host", "fcm_run_host_async",
+                  "fcm_run_unfused_static", "fcm_check", "fcm_plan",
                   "fcm_plan_desc", "fcm_tensor_bytes", "fcm_selftest_wait_timeout"):
             getattr(lib, f).restype = i
         lib.fcm_destroy.argtypes = [vp]
@@ -183,6 +186,11 @@ def fcm_run(handle: int, mode: int, inp: int, out: int, stream: int = 0) -> None
 
 def fcm_run_host(handle: int, mode: int, host_in: int, host_out: int, stream: int = 0) -> None:
     _check(load_library().fcm_run_host(handle, mode, host_in, host_out, stream))
+
+
+def fcm_run_host_async(handle: int, mode: int, host_in: int, host_out: int,
+                       stream: int = 0) -> None:
+    _check(load_library().fcm_run_host_async(handle, mode, host_in, host_out, stream))
 
 
 def fcm_run_unfused_static(handle: int, inp: int, out: int, stream: int = 0) -> None:
@@ -341,6 +349,17 @@ class FusedConvModule:
         s = (torch.cuda.current_stream().cuda_stream if stream is None
              else getattr(stream, "cuda_stream", stream))
         fcm_run_host(self.handle, m, host_in.data_ptr(), host_out.data_ptr(), s)
+
+    def run_host_async(self, host_in, host_out, mode: str | int = "fused", stream=None) -> None:
+        """fcm_run_host_async: enqueue without waiting; `host_out` holds the result once `stream`
+        has completed.  Keep both tensors alive and unchanged until then."""
+        import torch
+        m = MODES[mode] if isinstance(mode, str) else mode
+        check_run_buffers(self.mode_bytes, m, host_in, host_out, on_device=False)
+        s = (torch.cuda.current_stream().cuda_stream if stream is None
+             else getattr(stream, "cuda_stream", stream))
+        self._streams.add(s)
+        fcm_run_host_async(self.handle, m, host_in.data_ptr(), host_out.data_ptr(), s)
 
     def check(self, stream=None) -> None:
         import torch

@@ -95,6 +95,7 @@ static void free_handle(fcm_handle *h) {
     if (h->ev_start) cudaEventDestroy(h->ev_start);
     if (h->copy_in) cudaStreamDestroy(h->copy_in);
     if (h->copy_out) cudaStreamDestroy(h->copy_out);
+    if (h->compute) cudaStreamDestroy(h->compute);
     void *ptrs[] = {h->w1t, h->wpt, h->w1_raw, h->wp_img, h->w1_img, h->w1dw_img, h->w1dw_pad, h->s1, h->b1,
                     h->s2, h->b2, h->q1, h->i8_one, h->i8_zero, h->i8_idq, h->i8_idtap,
                     h->d_err, h->mid_buf, h->stage_in, h->stage_out};
@@ -348,9 +349,13 @@ static int host_chunks(const fcm_handle *h, int mode) {
     return h->d.n < 8 ? h->d.n : 8;
 }
 
-fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
-                        void *stream) {
-    FcmNvtxRange nvtx("fcm_run_host");
+// fcm_run_host and fcm_run_host_async.  `wait` = the synchronous entry point: the copies start
+// after the work already queued on `stream`, and the call returns once it has completed.
+// Otherwise the input copies are ordered only after this handle's previous host calls -- chunk
+// by chunk when the previous call split the batch the same way, so that its output copies
+// overlap this call's input copies -- and the call returns once the work is enqueued.
+static fcm_status run_host_impl(fcm_handle *h, int mode, const void *host_in, void *host_out,
+                                void *stream, bool wait) {
     if (!h) return fcm_fail(FCM_ERR_INVALID_ARG, "handle is NULL");
     if (!host_in || !host_out) return fcm_fail(FCM_ERR_INVALID_ARG, "host buffer is NULL");
     if (mode < FCM_MODE_FUSED || mode > FCM_MODE_UNFUSED)
@@ -358,10 +363,12 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
     size_t e = h->esize;
     size_t in_b = (mode == FCM_MODE_PW_ONLY ? h->m_elems : h->x_elems) * e;
     size_t out_b = (mode == FCM_MODE_CONV1_ONLY ? h->m_elems : h->y_elems) * e;
+    // (cudaFree waits for the device, so a staging buffer is never freed under a copy in flight)
     if (h->stage_in_bytes < in_b) {
         if (h->stage_in) cudaFree(h->stage_in);
         h->stage_in = nullptr;
         h->stage_in_bytes = 0;
+        h->host_prev_nch = 0;
         FCM_CUDA(cudaMalloc(&h->stage_in, in_b));
         h->stage_in_bytes = in_b;
     }
@@ -369,17 +376,21 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
         if (h->stage_out) cudaFree(h->stage_out);
         h->stage_out = nullptr;
         h->stage_out_bytes = 0;
+        h->host_prev_nch = 0;
         FCM_CUDA(cudaMalloc(&h->stage_out, out_b));
         h->stage_out_bytes = out_b;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int nch = host_chunks(h, mode);
     if (nch == 1) {
+        // everything on `stream`; a previous chunked call ended with `stream` waiting for its
+        // last output copy, so stream order covers the staging buffers
         FCM_CUDA(cudaMemcpyAsync(h->stage_in, host_in, in_b, cudaMemcpyHostToDevice, s));
         fcm_status st = fcm_run(h, mode, h->stage_in, h->stage_out, stream);
         if (st != FCM_OK) return st;
         FCM_CUDA(cudaMemcpyAsync(host_out, h->stage_out, out_b, cudaMemcpyDeviceToHost, s));
-        FCM_CUDA(cudaStreamSynchronize(s));
+        h->host_prev_nch = 1;
+        if (wait) FCM_CUDA(cudaStreamSynchronize(s));
         return FCM_OK;
     }
     // Pipelined over chunks of the batch: the input copy of chunk i+1 (copy_in stream), the
@@ -388,6 +399,7 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
     if (!h->copy_in) {
         FCM_CUDA(cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking));
         FCM_CUDA(cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking));
+        FCM_CUDA(cudaStreamCreateWithFlags(&h->compute, cudaStreamNonBlocking));
         FCM_CUDA(cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming));
         for (int i = 0; i < 8; i++) {
             FCM_CUDA(cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming));
@@ -395,10 +407,30 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
             FCM_CUDA(cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming));
         }
     }
-    // the copies start after the work already queued on the caller's stream
-    FCM_CUDA(cudaEventRecord(h->ev_start, s));
-    FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0));
-    FCM_CUDA(cudaStreamWaitEvent(h->copy_out, h->ev_start, 0));
+    const int prev = h->host_prev_nch;
+    const bool same_split = prev == nch && h->host_prev_mode == mode;
+    // the previous call's output copies may still be writing host memory this call reads
+    const char *prev_lo = static_cast<const char *>(h->host_prev_out);
+    const char *in_lo = static_cast<const char *>(host_in);
+    const bool in_overlaps_prev_out = prev > 1 && prev_lo && in_lo < prev_lo + h->host_prev_out_bytes &&
+                                      prev_lo < in_lo + in_b;
+    // The synchronous call runs its kernels on the caller's stream, after the work queued there.
+    // The asynchronous call runs them on the handle's compute stream, ordered chunk by chunk
+    // after the previous call's kernels and copies, so that the caller's stream only waits for
+    // the end of this call's copies out and the next call is not held up by it.
+    cudaStream_t ks = wait ? s : h->compute;
+    if (wait || prev == 1) {
+        // after the work already queued on the caller's stream (for the asynchronous call: the
+        // previous call ran its staging copies there)
+        FCM_CUDA(cudaEventRecord(h->ev_start, s));
+        FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0));
+        if (!wait) FCM_CUDA(cudaStreamWaitEvent(ks, h->ev_start, 0));
+    } else if (prev > 1 && !same_split) {
+        FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_run[prev - 1], 0));   // all its kernels
+        FCM_CUDA(cudaStreamWaitEvent(ks, h->ev_out[prev - 1], 0));           // all its copies out
+    }
+    if (!wait && in_overlaps_prev_out)
+        FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_out[prev - 1], 0));   // all its copies out
     const int n = h->d.n;
     const size_t in_img = in_b / n, out_img = out_b / n;
     int n0 = 0;
@@ -408,21 +440,46 @@ fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host
         char *hout = static_cast<char *>(host_out) + (size_t)n0 * out_img;
         char *din = static_cast<char *>(h->stage_in) + (size_t)n0 * in_img;
         char *dout = static_cast<char *>(h->stage_out) + (size_t)n0 * out_img;
+        if (!wait && same_split) {
+            // staging chunk i: its input is free once the previous call's kernel i has read it,
+            // its output once the previous call's copy out i is done (both waits are issued
+            // before this call records those events again)
+            FCM_CUDA(cudaStreamWaitEvent(h->copy_in, h->ev_run[i], 0));
+            FCM_CUDA(cudaStreamWaitEvent(ks, h->ev_out[i], 0));
+        }
         FCM_CUDA(cudaMemcpyAsync(din, hin, (size_t)nc * in_img, cudaMemcpyHostToDevice, h->copy_in));
         FCM_CUDA(cudaEventRecord(h->ev_in[i], h->copy_in));
-        FCM_CUDA(cudaStreamWaitEvent(s, h->ev_in[i], 0));
+        FCM_CUDA(cudaStreamWaitEvent(ks, h->ev_in[i], 0));
         fcm_handle v = batch_view(h, nc);
-        fcm_status st = run_one(&v, mode, din, dout, s);
+        fcm_status st = run_one(&v, mode, din, dout, ks);
         if (st != FCM_OK) return st;
-        FCM_CUDA(cudaEventRecord(h->ev_run[i], s));
+        FCM_CUDA(cudaEventRecord(h->ev_run[i], ks));
         FCM_CUDA(cudaStreamWaitEvent(h->copy_out, h->ev_run[i], 0));
         FCM_CUDA(cudaMemcpyAsync(hout, dout, (size_t)nc * out_img, cudaMemcpyDeviceToHost, h->copy_out));
         FCM_CUDA(cudaEventRecord(h->ev_out[i], h->copy_out));
         n0 += nc;
     }
+    // `stream` completes after the last output copy (copy_out runs its copies in order, each
+    // after its chunk's kernel)
     FCM_CUDA(cudaStreamWaitEvent(s, h->ev_out[nch - 1], 0));
-    FCM_CUDA(cudaStreamSynchronize(s));
+    h->host_prev_nch = nch;
+    h->host_prev_mode = mode;
+    h->host_prev_out = host_out;
+    h->host_prev_out_bytes = out_b;
+    if (wait) FCM_CUDA(cudaStreamSynchronize(s));
     return FCM_OK;
+}
+
+fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, void *host_out,
+                        void *stream) {
+    FcmNvtxRange nvtx("fcm_run_host");
+    return run_host_impl(h, mode, host_in, host_out, stream, true);
+}
+
+fcm_status fcm_run_host_async(fcm_handle *h, int mode, const void *host_in, void *host_out,
+                              void *stream) {
+    FcmNvtxRange nvtx("fcm_run_host_async");
+    return run_host_impl(h, mode, host_in, host_out, stream, false);
 }
 
 fcm_status fcm_check(fcm_handle *h, void *stream) {
@@ -449,6 +506,7 @@ void fcm_destroy(fcm_handle *h) {
     // the handle's own streams (fcm_run_host's copies); the caller's streams are the caller's
     if (h->copy_in) cudaStreamSynchronize(h->copy_in);
     if (h->copy_out) cudaStreamSynchronize(h->copy_out);
+    if (h->compute) cudaStreamSynchronize(h->compute);
     free_handle(h);
 }
 

@@ -98,8 +98,14 @@ struct fcm_handle {
     size_t stage_in_bytes = 0, stage_out_bytes = 0;
     // fcm_run_host pipelining: copy streams and per-chunk events (created on first use)
     cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaStream_t compute = nullptr;   // fcm_run_host_async's kernels
     cudaEvent_t ev_start = nullptr;
     cudaEvent_t ev_in[8] = {}, ev_run[8] = {}, ev_out[8] = {};
+    // the previous host call: chunks (0 = none, 1 = unsplit, on the caller's stream), mode and
+    // output buffer, which order fcm_run_host_async's copies after it
+    int host_prev_nch = 0, host_prev_mode = -1;
+    const void *host_prev_out = nullptr;
+    size_t host_prev_out_bytes = 0;
 };
 
 // thread-local last-error message (fcm_api.cu)
