@@ -197,7 +197,8 @@ FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, vo
  * `host_in` overlaps its `host_out`), but not after other work on `stream`: the caller orders
  * the producers of `host_in` itself.  Consecutive calls on one handle may therefore be in
  * flight together; they must come from one host thread.  Pinned host memory is required for
- * the copies to overlap. */
+ * the copies to overlap.  The batch is split into two chunks (not eight): calls in flight
+ * together overlap their copies anyway, and fewer copies cost less host time per call. */
 FCM_API fcm_status fcm_run_host_async(fcm_handle *h, int mode, const void *host_in,
                                       void *host_out, void *stream);
 

@@ -7,6 +7,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include <mutex>
 #include <vector>
 
@@ -381,7 +383,10 @@ static fcm_status run_host_impl(fcm_handle *h, int mode, const void *host_in, vo
         h->stage_out_bytes = out_b;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int nch = host_chunks(h, mode);
+    // The asynchronous call splits the batch in two: consecutive calls overlap their copies
+    // anyway, and fewer, larger copies cost less host time per call (MobileNet layer, calls
+    // back to back: 0.374 / 0.337 / 0.320 ms a call with 8 / 4 / 2 chunks).
+    const int nch = wait ? host_chunks(h, mode) : std::min(host_chunks(h, mode), 2);
     if (nch == 1) {
         // everything on `stream`; a previous chunked call ended with `stream` waiting for its
         // last output copy, so stream order covers the staging buffers

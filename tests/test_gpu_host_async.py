@@ -47,5 +47,18 @@ def test_async_calls_equal_sync_calls(cuda, name, n):
     stream.synchronize()
     for o, w in enumerate(want):
         assert np.array_equal(to_host(ys[o], wl.dtype), w), (name, o)
+    # a synchronous call between asynchronous ones (the batch split differently), then an
+    # asynchronous call reading the synchronous call's output
+    z1 = empty(wl.shapes()["y"], wl.dtype, "cpu", fill=float("nan")).pin_memory()
+    z2 = empty(wl.shapes()["y"], wl.dtype, "cpu", fill=float("nan")).pin_memory()
+    mod.run_host_async(xs[1], ys[0], "fused", stream=stream)
+    mod.run_host(xs[0], z1, "fused", stream=stream)
+    mod.run_host_async(z1, z2, "fused", stream=stream)
+    stream.synchronize()
+    assert np.array_equal(to_host(ys[0], wl.dtype), want[1])
+    assert np.array_equal(to_host(z1, wl.dtype), want[0])
+    ref = empty(wl.shapes()["y"], wl.dtype, "cpu", fill=float("nan")).pin_memory()
+    mod.run_host(z1, ref, "fused")
+    assert np.array_equal(to_host(z2, wl.dtype), to_host(ref, wl.dtype))
     mod.check(stream)
     mod.close()
