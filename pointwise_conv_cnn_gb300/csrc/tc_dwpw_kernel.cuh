@@ -531,16 +531,8 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                     emit16c(ra, std::integral_constant<int, C0>{});
                     emit16c(rb, std::integral_constant<int, C0 + 16>{});
                 };
-                static_assert(kEpiWarps == 8 || kEpiWarps == 4, "one or two epilogue warps per lane quadrant");
-                if (kEpiWarps == 4 && a.b2c_n == 128 && a.K == 128) {
-                    cols32(std::integral_constant<int, 0>{});
-                    cols32(std::integral_constant<int, 32>{});
-                    cols32(std::integral_constant<int, 64>{});
-                    cols32(std::integral_constant<int, 96>{});
-                } else if (kEpiWarps == 4 && a.b2c_n == 64 && a.K == 64) {
-                    cols32(std::integral_constant<int, 0>{});
-                    cols32(std::integral_constant<int, 32>{});
-                } else if (kEpiWarps == 8 && a.b2c_n == 128 && a.K == 128) {
+                static_assert(kEpiWarps == 8, "two epilogue warps per lane quadrant");
+                if (a.b2c_n == 128 && a.K == 128) {
                     if (part == 0) {
                         cols32(std::integral_constant<int, 0>{});
                         cols32(std::integral_constant<int, 32>{});
@@ -548,7 +540,7 @@ __global__ void __launch_bounds__(DWB == 2 ? kMaxThreadsBound2 : DWB ? kMaxThrea
                         cols32(std::integral_constant<int, 64>{});
                         cols32(std::integral_constant<int, 96>{});
                     }
-                } else if (kEpiWarps == 8 && a.b2c_n == 64 && a.K == 64) {
+                } else if (a.b2c_n == 64 && a.K == 64) {
                     if (part == 0)
                         cols32(std::integral_constant<int, 0>{});
                     else
