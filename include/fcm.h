@@ -181,7 +181,7 @@ FCM_API fcm_status fcm_run(fcm_handle *h, int mode, const void *in, void *out, v
 /* End-to-end variant of fcm_run on HOST buffers: copies `host_in` to a device staging buffer
  * owned by the handle (allocated on first use), runs `mode`, copies the result to `host_out`
  * and synchronizes `stream` before returning.  For batches of two or more images (all modes
- * but FCM_MODE_UNFUSED) the batch is split into up to 8 chunks whose input copies, kernels (on
+ * but FCM_MODE_UNFUSED) the batch is split into up to 6 chunks whose input copies, kernels (on
  * `stream`) and output copies overlap, using two copy streams the handle creates on first
  * use.  Pinned host memory makes the copies faster and lets them overlap; pageable memory
  * also works. */
@@ -197,7 +197,7 @@ FCM_API fcm_status fcm_run_host(fcm_handle *h, int mode, const void *host_in, vo
  * `host_in` overlaps its `host_out`), but not after other work on `stream`: the caller orders
  * the producers of `host_in` itself.  Consecutive calls on one handle may therefore be in
  * flight together; they must come from one host thread.  Pinned host memory is required for
- * the copies to overlap.  The batch is split into two chunks (not eight): calls in flight
+ * the copies to overlap.  The batch is split into two chunks (not six): calls in flight
  * together overlap their copies anyway, and fewer copies cost less host time per call. */
 FCM_API fcm_status fcm_run_host_async(fcm_handle *h, int mode, const void *host_in,
                                       void *host_out, void *stream);
