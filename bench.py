@@ -7,7 +7,11 @@ from serving them, each step uses the next of R input/output buffer sets whose t
 than twice the L2 size.
 
 Prints ONE JSON line (rank 0).  `value` is the achieved algorithmic HBM bandwidth (input +
-weights + scale/bias + output, each once) of the whole job; images/s is reported beside it.
+weights + scale/bias + output, each once) of the whole job over K steps launched back to back
+between two CUDA events (no event between launches, which would serialise them); images/s is
+reported beside it, and the spread of single launches from a separate untimed pass.  `e2e`
+measures the same bytes end to end from pinned host memory through fcm_run_host_async, every
+step's copies in and out inside the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--mode fused|unfused]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host cores
