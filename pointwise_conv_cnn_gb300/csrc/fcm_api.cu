@@ -229,6 +229,10 @@ fcm_status fcm_create(const fcm_desc *desc, const void *w1, const void *wp, cons
         memcpy(h->b2_host, hb2.data(), sizeof(float) * (size_t)K);
         h->b2_host_of = h->b2;
     }
+    if (cm <= 128) {
+        memcpy(h->b1_host, hb1.data(), sizeof(float) * (size_t)cm);
+        h->b1_host_of = h->b1;
+    }
     if (h->plan.kernel == FCM_KERNEL_TC) {
         st = fcm_tc_prepare(h, hw1.data(), hwp.data());
         if (st != FCM_OK) {

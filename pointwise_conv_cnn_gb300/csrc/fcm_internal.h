@@ -85,6 +85,8 @@ struct fcm_handle {
     // points to; the DW->PW role kernel passes them as kernel parameters
     float b2_host[128] = {};
     const float *b2_host_of = nullptr;
+    float b1_host[128] = {};          // the same for the first layer's biases (Cm <= 128)
+    const float *b1_host_of = nullptr;
     // INT8: 1152 * (sum of each channel's taps), and the identity stencil (one f16 tap of 1,
     // scale 1, bias 0, offset 1152) through which the PW-only mode runs on the fused kernel
     float *q1 = nullptr;
